@@ -1,0 +1,170 @@
+"""B300-native quantized linear projections (W4A4, W8A8, W4A16) for VLA PTQ.
+
+Thin Python binding over libvqlin.so.  Every function here only marshals
+arguments (device pointers, sizes, the current CUDA stream) and allocates
+output tensors with PyTorch; all arithmetic runs in the library's CUDA
+kernels.  The library has no CPU fallback: importing this package without
+the built library, or calling it on CPU tensors, raises.
+
+Tensor conventions (see include/vqlin.h):
+  * activations X [M, K] and weights W [N, K] are torch.bfloat16, row-major;
+  * int4 codes are uint8 [rows, K/2] (two's complement nibbles, even channel
+    in the low nibble); int8 codes are int8 [rows, K];
+  * per-token / per-channel scales are float32; W4A16 group scales and zero
+    points are bfloat16 [N, K/group].
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._abi import LIB_PATH, VqlinError, check, load  # noqa: F401
+
+__all__ = [
+    "VqlinError", "load", "LIB_PATH",
+    "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w8a8",
+    "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "get_last_device_error",
+]
+
+_lib = load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libvqlin has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def get_last_device_error(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a device error."""
+    check(_lib.vqlin_get_last_device_error(_stream(stream)), "vqlin_get_last_device_error")
+
+
+def quantize_weights_rtn(W, bits: int, symmetric: bool = True, group_size: int = 0,
+                         hadamard_block: int = 0, stream=None):
+    """Offline RTN of W [N, K] bf16.  Returns (q, s) or, asymmetric, (q, s, z)."""
+    _need(W, "W", torch.bfloat16, 2)
+    N, K = W.shape
+    dev = W.device
+    if bits == 4:
+        q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    else:
+        q = torch.empty((N, K), dtype=torch.int8, device=dev)
+    if symmetric:
+        s = torch.empty((N,), dtype=torch.float32, device=dev)
+        z = None
+    else:
+        G = K // group_size if group_size > 0 else 0
+        s = torch.empty((N, G), dtype=torch.bfloat16, device=dev)
+        z = torch.empty((N, G), dtype=torch.bfloat16, device=dev)
+    check(_lib.vqlin_quantize_weights_rtn(_ptr(W), N, K, bits, int(symmetric), group_size,
+                                          hadamard_block, _ptr(q), _ptr(s), _ptr(z), _stream(stream)),
+          "vqlin_quantize_weights_rtn")
+    return (q, s) if symmetric else (q, s, z)
+
+
+def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_out=None,
+                       scale_out=None, stream=None):
+    """Rotate X [M, K] bf16 block-wise and quantize per token.  Returns (q, s)."""
+    _need(X, "X", torch.bfloat16, 2)
+    M, K = X.shape
+    if q_out is None:
+        q_out = torch.empty((M, K // 2) if bits == 4 else (M, K),
+                            dtype=torch.uint8 if bits == 4 else torch.int8, device=X.device)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
+    if static_scale is not None:
+        _need(static_scale, "static_scale", torch.float32)
+    check(_lib.vqlin_act_hadamard_quant(_ptr(X), M, K, bits, hadamard_block, _ptr(static_scale),
+                                        _ptr(q_out), _ptr(scale_out), _stream(stream)),
+          "vqlin_act_hadamard_quant")
+    return q_out, scale_out
+
+
+def _linear_int(fn, what, xq, sx, wq, sw, bias, out, K, stream):
+    M, N = xq.shape[0], wq.shape[0]
+    _need(sx, "sx", torch.float32, 1)
+    _need(sw, "sw", torch.float32, 1)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    check(fn(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(bias), _ptr(out), M, N, K,
+             _stream(stream)), what)
+    return out
+
+
+def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int4 codes (uint8 [rows, K/2])."""
+    _need(xq, "xq", torch.uint8, 2)
+    _need(wq, "wq", torch.uint8, 2)
+    return _linear_int(_lib.vqlin_linear_w4a4, "vqlin_linear_w4a4", xq, sx, wq, sw, bias, out,
+                       xq.shape[1] * 2, stream)
+
+
+def linear_w8a8(xq, sx, wq, sw, bias=None, out=None, stream=None):
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int8 codes."""
+    _need(xq, "xq", torch.int8, 2)
+    _need(wq, "wq", torch.int8, 2)
+    return _linear_int(_lib.vqlin_linear_w8a8, "vqlin_linear_w8a8", xq, sx, wq, sw, bias, out,
+                       xq.shape[1], stream)
+
+
+def linear_w4a16(X, wq, scales, zeros, group_size: int = 128, bias=None, out=None, stream=None):
+    """Y = bf16(X . dequant(wq, scales, zeros)^T + bias), weight-only int4."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(wq, "wq", torch.uint8, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    _need(zeros, "zeros", torch.bfloat16, 2)
+    M, K = X.shape
+    N = wq.shape[0]
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    check(_lib.vqlin_linear_w4a16(_ptr(X), _ptr(wq), _ptr(scales), _ptr(zeros), group_size,
+                                  _ptr(bias), _ptr(out), M, N, K, _stream(stream)),
+          "vqlin_linear_w4a16")
+    return out
+
+
+def linear_bf16_ref(X, W, bias=None, out=None, stream=None):
+    """The 16-bit baseline Y = bf16(X . W^T + bias) (cuBLASLt)."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    M, K = X.shape
+    N = W.shape[0]
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    check(_lib.vqlin_linear_bf16_ref(_ptr(X), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                     _stream(stream)), "vqlin_linear_bf16_ref")
+    return out
+
+
+def debug_gemm_s32(bits: int, xq, wq, K: int, out=None, stream=None):
+    """int32 accumulators of the W4A4 (bits 4) / W8A8 (bits 8) integer GEMM."""
+    M, N = xq.shape[0], wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    check(_lib.vqlin_debug_gemm_s32(bits, _ptr(xq), _ptr(wq), _ptr(out), M, N, K, _stream(stream)),
+          "vqlin_debug_gemm_s32")
+    return out

@@ -1,0 +1,225 @@
+// Online activation kernel: block-Hadamard rotation + per-token quantization.
+//
+// Method: "FoldQuantVLA" abstract (block Hadamard transforms combined with
+// dynamic per-token quantization) and the "Omega-QVLA" technical summary
+// (normalised Hadamard matrix, applied block-wise over channels; per-step
+// static activation scales as the alternative to dynamic ones).
+//
+// Work decomposition (one pass over HBM, every value stays in registers):
+//   * a "unit" is 32 channels of one token held by one thread as four 8-channel
+//     chunks (one 128-bit load each);
+//   * a Hadamard block of b channels is spread over LPG = b/32 consecutive
+//     lanes: lane l of the block holds chunks l, l+LPG, l+2LPG, l+3LPG, so
+//     the 3 index bits inside a chunk and the 2 bits that pick the chunk are
+//     butterflied in registers and only log2(LPG) stages use warp shuffles;
+//   * the per-token absmax is reduced over the token's threads (shuffles, then
+//     shared memory across warps); one CTA holds one or more whole tokens.
+#include "common.cuh"
+
+namespace {
+
+using namespace vqlin_dev;
+
+constexpr int kThreads = 256;
+
+template <int HB>
+struct BlockGeom {
+  static constexpr int LPG = HB == 0 ? 1 : HB / 32;  // lanes per Hadamard block
+  static constexpr int G = 32 * LPG;                   // channels per lane group
+};
+
+__device__ __forceinline__ void butterfly(float& a, float& b) {
+  float s = a + b, d = a - b;
+  a = s;
+  b = d;
+}
+
+// Codes of one 8-channel chunk as packed int4 (one word) or int8 (two words).
+template <int BITS>
+__device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, float inv_s,
+                                               uint32_t& w0, uint32_t& w1) {
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  w0 = 0;
+  w1 = 0;
+  if (s == 0.0f) return;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // Fast quotient; near a rounding tie, redo with the IEEE division so the
+    // code equals rint(v / s) exactly (|t| <= 130 gives an error < 2^-10).
+    float t = v[e] * inv_s;
+    float rt = rintf(t);
+    if (fabsf(t - rt) > 0.4990234375f) rt = rintf(__fdiv_rn(v[e], s));
+    rt = fminf(fmaxf(rt, (float)(-qmax - 1)), (float)qmax);
+    int c = (int)rt;
+    if (BITS == 4) {
+      w0 |= (uint32_t)(c & 0xF) << (4 * e);
+    } else {
+      if (e < 4) w0 |= (uint32_t)(c & 0xFF) << (8 * e);
+      else w1 |= (uint32_t)(c & 0xFF) << (8 * (e - 4));
+    }
+  }
+}
+
+template <int BITS, int HB, int UPT>
+__global__ void __launch_bounds__(512)
+act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
+                 const float* __restrict__ static_scale, uint8_t* __restrict__ Q,
+                 float* __restrict__ S) {
+  using Geo = BlockGeom<HB>;
+  constexpr int LPG = Geo::LPG, G = Geo::G;
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  __shared__ float red[16];
+
+  const int r = threadIdx.x / tpr;  // token slot inside the CTA
+  const int ut = threadIdx.x % tpr;
+  const int m = blockIdx.x * rpc + r;
+  const bool row_ok = (r < rpc) && (m < M);
+  const int units = K / 32;
+  const int lane = threadIdx.x & 31;
+
+  float v[UPT][4][8];
+  float amax = 0.0f;
+  const uint16_t* xrow = X + (size_t)(row_ok ? m : 0) * K;
+
+#pragma unroll
+  for (int i = 0; i < UPT; ++i) {
+    const int u = ut + i * tpr;
+    const bool ok = row_ok && u < units;
+    const int g = u / LPG, l = u % LPG;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (ok) raw = ldg_nc_v4(xrow + (size_t)g * G + (l + LPG * j) * 8);
+      v[i][j][0] = bf16_lo(raw.x); v[i][j][1] = bf16_hi(raw.x);
+      v[i][j][2] = bf16_lo(raw.y); v[i][j][3] = bf16_hi(raw.y);
+      v[i][j][4] = bf16_lo(raw.z); v[i][j][5] = bf16_hi(raw.z);
+      v[i][j][6] = bf16_lo(raw.w); v[i][j][7] = bf16_hi(raw.w);
+    }
+    if (HB > 0) {
+      // index bits 0..2: inside the chunk
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if ((e & h) == 0) butterfly(v[i][j][e], v[i][j][e + h]);
+      }
+      // the two index bits above the lane bits: which of the 4 chunks
+#pragma unroll
+      for (int h = 1; h < 4; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((j & h) == 0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) butterfly(v[i][j][e], v[i][j + h][e]);
+      // lane bits: partner lane holds the other half of each butterfly
+#pragma unroll
+      for (int mk = 1; mk < LPG; mk <<= 1) {
+        const float sg = (lane & mk) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float p = __shfl_xor_sync(0xffffffffu, v[i][j][e], mk);
+            v[i][j][e] = fmaf(v[i][j][e], sg, p);
+          }
+      }
+      const float c = HB == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(b)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][j][e] *= c;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][j][e]));
+  }
+
+  float s;
+  if (static_scale != nullptr) {
+    s = __ldg(static_scale);
+  } else {
+    // per-token absmax over the token's tpr threads
+    if (tpr <= 32) {
+      for (int o = tpr >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) red[threadIdx.x >> 5] = amax;
+      __syncthreads();
+      const int wpr = tpr >> 5, w0 = r * wpr;
+      amax = 0.0f;
+      if (r < rpc)
+        for (int w = 0; w < wpr; ++w) amax = fmaxf(amax, red[w0 + w]);
+    }
+    s = __fdiv_rn(amax, (float)qmax);
+  }
+  if (!row_ok) return;
+  if (ut == 0) S[m] = s;
+  const float inv_s = s > 0.0f ? __frcp_rn(s) : 0.0f;
+
+#pragma unroll
+  for (int i = 0; i < UPT; ++i) {
+    const int u = ut + i * tpr;
+    if (u >= units) break;
+    const int g = u / LPG, l = u % LPG;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w0, w1;
+      quantize_chunk<BITS>(v[i][j], s, inv_s, w0, w1);
+      const size_t ch = (size_t)g * G + (l + LPG * j) * 8;  // first channel of the chunk
+      if (BITS == 4) {
+        *reinterpret_cast<uint32_t*>(Q + (size_t)m * (K / 2) + ch / 2) = w0;
+      } else {
+        *reinterpret_cast<uint2*>(Q + (size_t)m * K + ch) = make_uint2(w0, w1);
+      }
+    }
+  }
+}
+
+template <int BITS, int HB>
+cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, void* q, float* s,
+                      cudaStream_t st) {
+  const int units = K / 32;
+  const int upt = units <= 512 ? 1 : (units <= 1024 ? 2 : 4);  // at most 512 threads per token
+  int tpr = (units + upt - 1) / upt;
+  // threads per token: a power of two up to a warp, else whole warps
+  if (tpr <= 32) {
+    int p = 1;
+    while (p < tpr) p <<= 1;
+    tpr = p;
+  } else {
+    tpr = (tpr + 31) / 32 * 32;
+  }
+  const int rpc = tpr >= kThreads ? 1 : kThreads / tpr;
+  const int threads = rpc * tpr;
+  const unsigned grid = vqlin::ceil_div(M, rpc);
+  if (upt == 1)
+    act_quant_kernel<BITS, HB, 1><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
+  else if (upt == 2)
+    act_quant_kernel<BITS, HB, 2><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
+  else
+    act_quant_kernel<BITS, HB, 4><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace vqlin {
+
+cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
+                             const float* static_scale, void* q, float* s, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  if (bits == 4) {
+    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, q, s, st);
+    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, q, s, st);
+    return launch_hb<4, 128>(X, M, K, static_scale, q, s, st);
+  }
+  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, q, s, st);
+  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, q, s, st);
+  return launch_hb<8, 128>(X, M, K, static_scale, q, s, st);
+}
+
+}  // namespace vqlin

