@@ -55,7 +55,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         return _lib
     if not os.path.exists(path):
         raise ImportError(
-            f"{path} is missing: build it with `python -m bit_ptq_linear_vqlin_b300.build` "
+            f"{path} is missing: build it with `python bit_ptq_linear_vqlin_b300/build.py` "
             "(the library has no CPU fallback)")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():

@@ -4,7 +4,10 @@ Each .cu file is compiled to an object under <repo>/_build/ (in parallel,
 skipped when the object is newer than every source and header), then linked
 into bit_ptq_linear_vqlin_b300/libvqlin.so next to this file.
 
-    python -m bit_ptq_linear_vqlin_b300.build [--force] [--verbose]
+    python bit_ptq_linear_vqlin_b300/build.py [--force] [--verbose] [--ptxas-verbose]
+
+It is run by path (not as a package module) because importing the package
+loads the library it builds.
 """
 from __future__ import annotations
 
