@@ -317,8 +317,7 @@ class ControlStepStack:
 
         # ---- reusable code / scale / output buffers (one set per group shape)
         def codes(M, K, bits):
-            return torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8 if bits == 4 else torch.int8,
-                               device=dev)
+            return torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=dev)
         self.pre_buf = [dict(xq=codes(self.M_pre, g["K"], g["bits"]), sx=torch.empty(self.M_pre, device=dev),
                              y=torch.empty((self.M_pre, g["N"]), dtype=torch.bfloat16, device=dev))
                         for g in self.pre_groups]
@@ -741,12 +740,9 @@ def run_shape(args):
         return torch.randn((r, c), generator=g, device=dev).to(torch.bfloat16)
 
     def rand_codes(r, c, bits):
-        lo, hi = (-8, 8) if bits == 4 else (-128, 128)
-        t = torch.randint(lo, hi, (r, c), generator=g, device=dev, dtype=torch.int32)
-        if bits == 8:
-            return t.to(torch.int8)
-        t = t & 0xF
-        return (t[:, 0::2] | (t[:, 1::2] << 4)).to(torch.uint8)
+        # every byte is a valid sign-magnitude code (a negative zero reads as 0)
+        return torch.randint(0, 256, (r, c // 2 if bits == 4 else c), generator=g, device=dev,
+                             dtype=torch.int32).to(torch.uint8)
 
     group = 128
     if kind.startswith("act_quant"):
@@ -754,7 +750,7 @@ def run_shape(args):
         per = 2 * M * K
         flops, nbytes = 0, 2 * M * K + M * K * bits // 8 + 4 * M
         mk = lambda: dict(X=rand_bf16(M, K))  # noqa: E731
-        q = torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8 if bits == 4 else torch.int8, device=dev)
+        q = torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=dev)
         sx = torch.empty(M, device=dev)
         run = lambda d: vq.act_hadamard_quant(d["X"], bits, 128, q_out=q, scale_out=sx)  # noqa: E731
     elif kind in ("linear_w4a4", "linear_w8a8"):

@@ -8,8 +8,9 @@ the built library, or calling it on CPU tensors, raises.
 
 Tensor conventions (see include/vqlin.h):
   * activations X [M, K] and weights W [N, K] are torch.bfloat16, row-major;
-  * int4 codes are uint8 [rows, K/2] (two's complement nibbles, even channel
-    in the low nibble); int8 codes are int8 [rows, K];
+  * symmetric codes lie in [-qmax, qmax] and are sign-magnitude bytes held
+    in torch.uint8: int4 codes [rows, K/2] (nibble (c < 0) << 3 | |c|, even
+    channel in the low nibble), int8 codes [rows, K] (byte (c < 0) << 7 | |c|);
   * per-token / per-channel scales are float32; W4A16 group scales and zero
     points are bfloat16 [N, K/group].
 """
@@ -24,7 +25,8 @@ from ._abi import LIB_PATH, VqlinError, check, load  # noqa: F401
 __all__ = [
     "VqlinError", "load", "LIB_PATH",
     "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w8a8",
-    "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "get_last_device_error",
+    "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_withheld_loads",
+    "get_last_device_error",
 ]
 
 _lib = load()
@@ -63,10 +65,7 @@ def quantize_weights_rtn(W, bits: int, symmetric: bool = True, group_size: int =
     _need(W, "W", torch.bfloat16, 2)
     N, K = W.shape
     dev = W.device
-    if bits == 4:
-        q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
-    else:
-        q = torch.empty((N, K), dtype=torch.int8, device=dev)
+    q = torch.empty((N, K // 2) if bits == 4 else (N, K), dtype=torch.uint8, device=dev)
     if symmetric:
         s = torch.empty((N,), dtype=torch.float32, device=dev)
         z = None
@@ -86,8 +85,7 @@ def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_o
     _need(X, "X", torch.bfloat16, 2)
     M, K = X.shape
     if q_out is None:
-        q_out = torch.empty((M, K // 2) if bits == 4 else (M, K),
-                            dtype=torch.uint8 if bits == 4 else torch.int8, device=X.device)
+        q_out = torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=X.device)
     if scale_out is None:
         scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
     if static_scale is not None:
@@ -120,9 +118,9 @@ def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
 
 
 def linear_w8a8(xq, sx, wq, sw, bias=None, out=None, stream=None):
-    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int8 codes."""
-    _need(xq, "xq", torch.int8, 2)
-    _need(wq, "wq", torch.int8, 2)
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int8 codes (uint8 [rows, K])."""
+    _need(xq, "xq", torch.uint8, 2)
+    _need(wq, "wq", torch.uint8, 2)
     return _linear_int(_lib.vqlin_linear_w8a8, "vqlin_linear_w8a8", xq, sx, wq, sw, bias, out,
                        xq.shape[1], stream)
 
@@ -167,4 +165,17 @@ def debug_gemm_s32(bits: int, xq, wq, K: int, out=None, stream=None):
         out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
     check(_lib.vqlin_debug_gemm_s32(bits, _ptr(xq), _ptr(wq), _ptr(out), M, N, K, _stream(stream)),
           "vqlin_debug_gemm_s32")
+    return out
+
+
+def debug_gemm_withheld_loads(bits: int, xq, wq, K: int, limit_ns: int, out=None, stream=None):
+    """Failure-detection test: launch the integer GEMM with every tile load
+    withheld, so its bounded waits run out after limit_ns.  The error is then
+    raised by get_last_device_error()."""
+    M, N = xq.shape[0], wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    check(_lib.vqlin_debug_gemm_withheld_loads(bits, _ptr(xq), _ptr(wq), _ptr(out), M, N, K,
+                                               ctypes.c_uint64(limit_ns), _stream(stream)),
+          "vqlin_debug_gemm_withheld_loads")
     return out

@@ -36,6 +36,7 @@ SIGNATURES = {
     "vqlin_linear_w4a16": (_i, [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_bf16_ref": (_i, [_p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_debug_gemm_s32": (_i, [_i, _p, _p, _p, _i, _i, _i, _p]),
+    "vqlin_debug_gemm_withheld_loads": (_i, [_i, _p, _p, _p, _i, _i, _i, ctypes.c_uint64, _p]),
 }
 
 _lib = None

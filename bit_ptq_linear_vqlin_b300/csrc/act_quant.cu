@@ -34,7 +34,9 @@ __device__ __forceinline__ void butterfly(float& a, float& b) {
   b = d;
 }
 
-// Codes of one 8-channel chunk as packed int4 (one word) or int8 (two words).
+// Codes of one 8-channel chunk as sign-magnitude int4 (one word: nibble
+// (c < 0) << 3 | |c|, even channel low) or int8 (two words: byte
+// (c < 0) << 7 | |c|).
 template <int BITS>
 __device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, float inv_s,
                                                uint32_t& w0, uint32_t& w1) {
@@ -49,13 +51,15 @@ __device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, flo
     float t = v[e] * inv_s;
     float rt = rintf(t);
     if (fabsf(t - rt) > 0.4990234375f) rt = rintf(__fdiv_rn(v[e], s));
-    rt = fminf(fmaxf(rt, (float)(-qmax - 1)), (float)qmax);
-    int c = (int)rt;
+    rt = fminf(fmaxf(rt, (float)(-qmax)), (float)qmax);
+    const uint32_t mag = (uint32_t)fabsf(rt);
+    const uint32_t neg = rt < 0.0f ? 1u : 0u;
     if (BITS == 4) {
-      w0 |= (uint32_t)(c & 0xF) << (4 * e);
+      w0 |= ((neg << 3) | mag) << (4 * e);
     } else {
-      if (e < 4) w0 |= (uint32_t)(c & 0xFF) << (8 * e);
-      else w1 |= (uint32_t)(c & 0xFF) << (8 * (e - 4));
+      const uint32_t b = (neg << 7) | mag;
+      if (e < 4) w0 |= b << (8 * e);
+      else w1 |= b << (8 * (e - 4));
     }
   }
 }

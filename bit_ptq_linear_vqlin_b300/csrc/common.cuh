@@ -29,10 +29,16 @@ cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, i
                                     void* q, float* s, cudaStream_t st);
 cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
                                      uint8_t* q, uint16_t* s, uint16_t* z, cudaStream_t st);
-// Integer GEMM; mode 0 = bf16 epilogue into Y, mode 1 = raw int32 into acc.
-cudaError_t launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq,
-                            const float* sw, const uint16_t* bias, uint16_t* Y, int32_t* acc,
-                            int M, int N, int K, int* status, cudaStream_t st);
+// Integer GEMM (tcgen05); acc == nullptr: bf16 epilogue into Y, else raw int32
+// accumulators into acc.
+vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq,
+                             const float* sw, const uint16_t* bias, uint16_t* Y, int32_t* acc,
+                             int M, int N, int K, int* status, cudaStream_t st);
+// The same GEMM with its producer withholding every tile load, so that the
+// consumers' bounded waits run out after limit_ns (failure-detection test).
+vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, int32_t* acc,
+                                      int M, int N, int K, int* status, uint64_t limit_ns,
+                                      cudaStream_t st);
 cudaError_t launch_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
                          const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
                          int M, int N, int K, int* status, cudaStream_t st);
@@ -40,6 +46,8 @@ cudaError_t launch_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* s
 // Largest K each kernel supports (host-side shape checks).
 constexpr int kActQuantMaxK = 65536;
 constexpr int kWeightQuantMaxK = 49152;
+constexpr int kGemmW4MaxK = 65536;   // |acc| <= 49 K stays below 2^24
+constexpr int kGemmW8MaxK = 16384;   // 1024 channels per CTA x 16 CTAs per cluster
 
 }  // namespace vqlin
 

@@ -1,0 +1,412 @@
+// Integer GEMM of the W4A4 / W8A8 projections on the tcgen05 tensor cores.
+//
+//   acc[m, n] = sum_k xq[m, k] * wq[n, k]        (exact int32)
+//   Y[m, n]   = bf16(((float)acc * sx[m]) * sw[n] + bias[n])
+//
+// Method: "FoldQuantVLA" abstract (W4A4 projections executed natively in
+// integers after per-token activation and per-channel weight quantization;
+// attention-output and FFN-down projections kept at W8A8).
+//
+// sm_103a has no integer tcgen05 MMA, so the integer codes ride in floating
+// point operands whose products and sums are exact:
+//   * int4 code c (sign-magnitude nibble s|mmm, |c| <= 7) is the e4m3 subnormal
+//     byte s<<7 | mmm, value c * 2^-9; the MMA is kind::f8f6f4 and the float32
+//     accumulator holds acc * 2^-18 exactly (|acc| <= 49 K < 2^24 for K < 342k);
+//   * int8 code c (sign-magnitude byte, |c| <= 127) is the f16 subnormal
+//     s<<15 | |c|, value c * 2^-24; the MMA is kind::f16 and the accumulator
+//     holds acc * 2^-48 exactly while |acc| <= 127^2 * 1024 < 2^24, so every CTA
+//     sums at most 1024 channels and longer K is split across the cluster.
+// Conversions are a few bit operations per 32-bit word (no lookup table).
+//
+// Work decomposition (swap-AB: weights are the MMA's M side):
+//   * one CTA computes 128 output channels x BT tokens (BT <= 256, a multiple
+//     of 16) over a range of K; grid = (N/128, M/BT, S) with the S CTAs that
+//     share an output tile forming one thread-block cluster (split K);
+//   * warp 0: TMA producer of the packed code tiles (weights and activations,
+//     64 bytes of each row per k-block) into a ring of raw stages;
+//   * warps 2..5: unpack each raw stage into the MMA operand layout (128-byte
+//     swizzled K-major rows) in a ring of operand stages;
+//   * warp 1: allocates tensor memory and issues the MMAs (one thread), 4 per
+//     k-block, accumulating 128 x BT float32 in tensor memory;
+//   * epilogue: warps 2..5 convert the accumulator to int32 in shared memory;
+//     after a cluster barrier each CTA of the cluster sums its slice of the
+//     output channels over the cluster's shared memory (DSMEM) and applies the
+//     scale epilogue, so split K needs no global scratch memory and the sum
+//     is deterministic.
+// Every wait is bounded in time; a wait that runs out records
+// VQLIN_ERR_TIMEOUT in the device status word and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+using namespace vqlin_dev;
+
+constexpr int kTileN = 128;       // output channels per CTA (MMA M)
+constexpr int kRawRow = 64;       // packed bytes of one row per k-block
+constexpr int kOpRow = 128;       // operand bytes of one row per k-block
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kUnpackThreads = 128;
+constexpr int kMaxSplit = 16;
+constexpr int kOpStages = 2;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+struct QgemmArgs {
+  const float* sx;
+  const float* sw;
+  const uint16_t* bias;
+  uint16_t* Y;
+  int32_t* acc;          // non-null: store raw int32 accumulators instead of Y
+  int* status;
+  int M, N, K;           // K in codes
+  int bt;                // token tile
+  int nkb;               // k-blocks over K
+  int raw_stages;
+  uint32_t tmem_cols;
+  uint64_t wait_limit_ns;
+  int withhold_loads;    // test hook: the producer issues nothing (waits run out)
+};
+
+// Unpacks 8 packed bytes into 16 operand bytes.
+//   int4: word w holds channels 0..7 (nibble s|mmm, even channel low).  The
+//   e4m3 bytes of the even channels are (w & 0x07070707) | ((w << 4) &
+//   0x80808080) and of the odd channels ((w >> 4) & 0x07070707) |
+//   (w & 0x80808080); the chunk's channel order becomes 0,2,4,6,1,3,5,7, the
+//   same permutation on both operands, which leaves every dot product
+//   unchanged.
+//   int8: byte s|mmmmmmm -> f16 s<<15 | mmmmmmm: prmt copies the byte and
+//   replicates its sign bit into the high byte, a mask keeps bit 15 and 0..6.
+template <int BITS>
+__device__ __forceinline__ uint4 unpack8(uint2 in) {
+  uint4 o;
+  if (BITS == 4) {
+    o.x = (in.x & 0x07070707u) | ((in.x << 4) & 0x80808080u);
+    o.y = ((in.x >> 4) & 0x07070707u) | (in.x & 0x80808080u);
+    o.z = (in.y & 0x07070707u) | ((in.y << 4) & 0x80808080u);
+    o.w = ((in.y >> 4) & 0x07070707u) | (in.y & 0x80808080u);
+  } else {
+    o.x = __byte_perm(in.x, 0u, 0x9180) & 0x807F807Fu;
+    o.y = __byte_perm(in.x, 0u, 0xB3A2) & 0x807F807Fu;
+    o.z = __byte_perm(in.y, 0u, 0x9180) & 0x807F807Fu;
+    o.w = __byte_perm(in.y, 0u, 0xB3A2) & 0x807F807Fu;
+  }
+  return o;
+}
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, 0, (int)VQLIN_ERR_TIMEOUT);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+             const QgemmArgs a) {
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const int bt = a.bt;
+  const int rows = kTileN + bt;
+  const uint32_t op_bytes = (uint32_t)rows * kOpRow;
+  const uint32_t raw_bytes = (uint32_t)rows * kRawRow;
+  const int R = a.raw_stages;
+  uint8_t* op = base;
+  uint8_t* raw = base + kOpStages * op_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (size_t)R * raw_bytes);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = bars + R;
+  uint64_t* op_full = bars + 2 * R;
+  uint64_t* op_empty = bars + 2 * R + kOpStages;
+  uint64_t* acc_full = bars + 2 * R + 2 * kOpStages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = (int)gridDim.z;
+  const uint32_t rank = cluster_ctarank();
+  const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * bt;
+  const int kb0 = (int)(((long long)rank * a.nkb) / S);
+  const int kb1 = (int)(((long long)(rank + 1) * a.nkb) / S);
+  const int cnt = kb1 - kb0;
+  volatile int* abort = &s_abort;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kUnpackThreads);
+    }
+    for (int i = 0; i < kOpStages; ++i) {
+      mbar_init(&op_full[i], kUnpackThreads);
+      mbar_init(&op_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init_fence();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      if (!a.withhold_loads) {
+        for (int i = 0; i < cnt; ++i) {
+          const int s = i % R;
+          if (i >= R && !mbar_wait_bounded(&raw_empty[s], ((i / R) - 1) & 1, a.wait_limit_ns, abort)) {
+            if (!*abort) record_timeout(a.status, abort);
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[s], raw_bytes);
+          uint8_t* dst = raw + (size_t)s * raw_bytes;
+          tma_load_2d(dst, &tmW, (kb0 + i) * kRawRow, n0, &raw_full[s]);
+          tma_load_2d(dst + kTileN * kRawRow, &tmX, (kb0 + i) * kRawRow, m0, &raw_full[s]);
+          ++issued;
+        }
+      }
+      // copies still in flight complete before the CTA may exit
+      for (int i = issued > R ? issued - R : 0; i < issued; ++i)
+        if (!mbar_wait_bounded(&raw_full[i % R], (i / R) & 1, a.wait_limit_ns, nullptr))
+          record_timeout(a.status, abort);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f32acc(0u, kTileN, 0) ;
+      const uint32_t id = idesc | ((uint32_t)(bt >> 3) << 17);
+      for (int i = 0; i < cnt; ++i) {
+        const int ps = i % kOpStages;
+        if (!mbar_wait_bounded(&op_full[ps], (i / kOpStages) & 1, a.wait_limit_ns, abort)) {
+          if (!*abort) record_timeout(a.status, abort);
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* st = op + (size_t)ps * op_bytes;
+        const uint64_t da = sdesc_sw128(st), db = sdesc_sw128(st + kTileN * kOpRow);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // +32 bytes along K inside the 128-byte swizzled row per MMA
+          if (BITS == 4) mma_f8f6f4(tmem, da + 2 * j, db + 2 * j, id, (i | j) != 0);
+          else mma_f16(tmem, da + 2 * j, db + 2 * j, id, (i | j) != 0);
+        }
+        tc_commit(&op_empty[ps]);
+      }
+      tc_commit(acc_full);
+    }
+  } else {
+    // ------------------------------------------------------------ unpackers
+    const int t = tid - 64;
+    for (int i = 0; i < cnt; ++i) {
+      const int s = i % R, ps = i % kOpStages;
+      if (!mbar_wait_bounded(&raw_full[s], (i / R) & 1, a.wait_limit_ns, abort)) {
+        if (!*abort) record_timeout(a.status, abort);
+        break;
+      }
+      if (i >= kOpStages &&
+          !mbar_wait_bounded(&op_empty[ps], ((i / kOpStages) - 1) & 1, a.wait_limit_ns, abort)) {
+        if (!*abort) record_timeout(a.status, abort);
+        break;
+      }
+      const uint8_t* rs = raw + (size_t)s * raw_bytes;
+      uint8_t* os = op + (size_t)ps * op_bytes;
+      for (int task = t; task < rows * 8; task += kUnpackThreads) {
+        const int r = task >> 3, c = task & 7;
+        const uint2 w = *reinterpret_cast<const uint2*>(rs + r * kRawRow + c * 8);
+        *reinterpret_cast<uint4*>(os + r * kOpRow + ((c ^ (r & 7)) << 4)) = unpack8<BITS>(w);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&raw_empty[s]);
+      mbar_arrive(&op_full[ps]);
+    }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  // The int32 partial tile [128 channels][bt tokens] (row stride bt + 1 words)
+  // overlays the operand and raw rings, which are idle once acc_full completes.
+  __syncwarp();  // the single-thread roles rejoin their warps
+  int32_t* part = reinterpret_cast<int32_t*>(base);
+  const int ldp = bt + 1;
+  if (warp >= 2) {
+    const bool ok = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, nullptr);
+    if (!ok) record_timeout(a.status, abort);
+    tc_fence_after();
+    // warp-uniform decision: the tensor-memory loads below are warp-collective
+    if (__all_sync(0xffffffffu, ok && !*abort)) {
+      const int q = warp & 3;              // tensor-memory lane quadrant of this warp
+      const int row = q * 32 + lane;       // output channel inside the tile
+      const float unit = BITS == 4 ? 262144.0f : 281474976710656.0f;  // 2^18, 2^48
+      for (int c0 = 0; c0 < bt; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          part[row * ldp + c0 + j] = __float2int_rn(__uint_as_float(v[j]) * unit);
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();
+
+  if (!*abort) {
+    const int rows_per = (kTileN + S - 1) / S;
+    const int r0 = (int)rank * rows_per;
+    const int r1 = min(kTileN, r0 + rows_per);
+    const int nr = r1 - r0;
+    if (nr > 0) {
+      const uint32_t part_s = smem_addr(part);
+      for (int idx = tid; idx < nr * bt; idx += kThreads) {
+        const int rr = r0 + idx % nr, col = idx / nr;
+        const int n = n0 + rr, m = m0 + col;
+        if (n >= a.N || m >= a.M) continue;
+        const uint32_t off = (uint32_t)(rr * ldp + col) * 4u;
+        int32_t sum = 0;
+        for (int c = 0; c < S; ++c) sum += ld_shared_cluster_s32(mapa_shared(part_s + off, (uint32_t)c));
+        if (a.acc != nullptr) {
+          a.acc[(size_t)m * a.N + n] = sum;
+        } else {
+          float y = __fmul_rn(__fmul_rn((float)sum, __ldg(a.sx + m)), __ldg(a.sw + n));
+          if (a.bias != nullptr) y = __fadd_rn(y, __uint_as_float((uint32_t)__ldg(a.bias + n) << 16));
+          a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(y);
+        }
+      }
+    }
+  }
+  cluster_sync_all();  // peers have finished reading this CTA's shared memory
+  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a [rows, row_bytes] uint8 matrix, box = 64 bytes x box_rows,
+// no swizzle; out-of-range rows read as zero.
+bool make_tmap(CUtensorMap* tm, const void* ptr, int rows, int row_bytes, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kRawRow, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 227 KB opt-in per CTA, less room for the kernel's static shared memory
+constexpr int kMaxSmem = 232448 - 1024;
+
+size_t smem_bytes(int bt, int raw_stages) {
+  const size_t rows = kTileN + bt;
+  return 1024 + kOpStages * rows * kOpRow + raw_stages * rows * kRawRow + (2 * raw_stages + 2 * kOpStages + 1) * 8;
+}
+
+template <int BITS>
+vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
+                         uint16_t* Y, int32_t* acc, int M, int N, int K, int* status, int withhold,
+                         uint64_t limit_ns, cudaStream_t st) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(qgemm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(qgemm_kernel<BITS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr_err != cudaSuccess)
+    return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+
+  const int kb_codes = BITS == 4 ? 128 : 64;
+  const int row_bytes = BITS == 4 ? K / 2 : K;
+  const int nt = (M + 255) / 256;
+  const int bt = ((M + nt - 1) / nt + 15) / 16 * 16;
+  const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + bt - 1) / bt;
+  const int nkb = K / kb_codes;
+  const int s_min = BITS == 8 ? (K + 1023) / 1024 : 1;
+  int S = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
+  S = S < s_min ? s_min : S;
+  S = S > kMaxSplit ? kMaxSplit : S;
+  S = S > nkb ? nkb : S;
+  if (S < s_min)  // host checks keep K <= 16384 for int8
+    return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: K=%d needs %d-way split", K, s_min);
+  const int per_cta = (nkb + S - 1) / S;
+  // raw stages: up to 6 within the shared-memory limit, no more than the
+  // k-blocks a CTA runs, at least 2 (the int32 partial tile of the epilogue
+  // overlays the rings and needs 2 raw stages' room for bt <= 256)
+  int R = 6;
+  while (R > 2 && smem_bytes(bt, R) > (size_t)kMaxSmem) --R;
+  if (R > per_cta) R = per_cta < 2 ? 2 : per_cta;
+  uint32_t cols = 32;
+  while ((int)cols < bt) cols <<= 1;
+
+  CUtensorMap tmW, tmX;
+  if (!encode_fn()) return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cuTensorMapEncodeTiled is unavailable");
+  if (!make_tmap(&tmW, wq, N, row_bytes, kTileN) || !make_tmap(&tmX, xq, M, row_bytes, bt))
+    return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
+
+  QgemmArgs a;
+  a.sx = sx; a.sw = sw; a.bias = bias; a.Y = Y; a.acc = acc; a.status = status;
+  a.M = M; a.N = N; a.K = K; a.bt = bt; a.nkb = nkb; a.raw_stages = R; a.tmem_cols = cols;
+  a.wait_limit_ns = limit_ns; a.withhold_loads = withhold;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_m, S);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(bt, R);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = S;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, qgemm_kernel<BITS>, tmW, tmX, a);
+  if (e != cudaSuccess)
+    return vqlin::fail(VQLIN_ERR_CUDA, "qgemm launch (grid %d x %d x %d, cluster %d, %zu B smem): %s", tiles_n,
+                       tiles_m, S, S, cfg.dynamicSmemBytes, cudaGetErrorString(e));
+  return VQLIN_OK;
+}
+
+}  // namespace
+
+namespace vqlin {
+
+vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq, const float* sw,
+                             const uint16_t* bias, uint16_t* Y, int32_t* acc, int M, int N, int K, int* status,
+                             cudaStream_t st) {
+  if (M == 0 || N == 0) return VQLIN_OK;
+  if (bits == 4) return launch_bits<4>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
+  return launch_bits<8>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
+}
+
+vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, int32_t* acc, int M, int N, int K,
+                                     int* status, uint64_t limit_ns, cudaStream_t st) {
+  if (bits == 4) return launch_bits<4>(xq, nullptr, wq, nullptr, nullptr, nullptr, acc, M, N, K, status, 1, limit_ns, st);
+  return launch_bits<8>(xq, nullptr, wq, nullptr, nullptr, nullptr, acc, M, N, K, status, 1, limit_ns, st);
+}
+
+}  // namespace vqlin

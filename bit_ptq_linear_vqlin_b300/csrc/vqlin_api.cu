@@ -99,7 +99,7 @@ using vqlin::fail;
 
 extern "C" {
 
-int vqlin_version(void) { return 100; }
+int vqlin_version(void) { return 200; }
 
 const char* vqlin_status_string(vqlin_status s) {
   switch (s) {
@@ -193,7 +193,9 @@ static vqlin_status linear_int(int bits, const void* xq, const float* sx, const 
                                void* stream) {
   REQUIRE(M >= 0 && N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
   const int kmul = bits == 4 ? 128 : 64;
+  const int kmax = bits == 4 ? vqlin::kGemmW4MaxK : vqlin::kGemmW8MaxK;
   REQUIRE(K % kmul == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of %d", K, kmul);
+  REQUIRE(K <= kmax, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K, kmax);
   if (M == 0 || N == 0) return VQLIN_OK;
   REQUIRE_PTR(xq); REQUIRE_PTR(wq);
   REQUIRE_ALIGNED(xq); REQUIRE_ALIGNED(wq);
@@ -205,9 +207,8 @@ static vqlin_status linear_int(int bits, const void* xq, const float* sx, const 
   }
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
-  return vqlin::check_launch(vqlin::launch_int_gemm(bits, xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
-                                                    static_cast<cudaStream_t>(stream)),
-                             bits == 4 ? "linear_w4a4" : "linear_w8a8");
+  return vqlin::launch_int_gemm(bits, xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
+                                static_cast<cudaStream_t>(stream));
 }
 
 vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
@@ -215,7 +216,7 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
   return linear_int(4, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
 }
 
-vqlin_status vqlin_linear_w8a8(const int8_t* xq, const float* sx, const int8_t* wq, const float* sw,
+vqlin_status vqlin_linear_w8a8(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                const uint16_t* bias, uint16_t* Y, int M, int N, int K, void* stream) {
   return linear_int(8, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
 }
@@ -225,6 +226,22 @@ vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int3
   REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
   REQUIRE_PTR(acc);
   return linear_int(bits, xq, nullptr, wq, nullptr, nullptr, nullptr, acc, M, N, K, stream);
+}
+
+vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const void* wq, int32_t* acc, int M,
+                                             int N, int K, uint64_t limit_ns, void* stream) {
+  REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
+  REQUIRE(M > 0 && N > 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
+  const int kmul = bits == 4 ? 128 : 64;
+  const int kmax = bits == 4 ? vqlin::kGemmW4MaxK : vqlin::kGemmW8MaxK;
+  REQUIRE(K % kmul == 0 && K <= kmax, VQLIN_ERR_UNSUPPORTED_SHAPE, "unsupported K=%d", K);
+  REQUIRE(limit_ns > 0 && limit_ns <= 2000000000ull, VQLIN_ERR_INVALID_ARG, "limit_ns must be in (0, 2e9]");
+  REQUIRE_PTR(xq); REQUIRE_PTR(wq); REQUIRE_PTR(acc);
+  REQUIRE_ALIGNED(xq); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(acc);
+  int* status = vqlin::device_status_word();
+  REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
+  return vqlin::launch_int_gemm_withheld(bits, xq, wq, acc, M, N, K, status, limit_ns,
+                                         static_cast<cudaStream_t>(stream));
 }
 
 vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,

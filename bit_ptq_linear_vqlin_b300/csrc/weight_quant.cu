@@ -69,18 +69,19 @@ weight_quant_sym_kernel(const uint16_t* __restrict__ W, int K, int hb, uint8_t* 
 
   // each thread quantizes pairs of channels (one int4 byte or two int8 bytes)
   for (int k = 2 * t; k < K; k += 2 * kSymThreads) {
-    int c[2];
+    // sign-magnitude codes in [-qmax, qmax]: nibble (c < 0) << 3 | |c| or
+    // byte (c < 0) << 7 | |c|
+    uint32_t c[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float r = s > 0.0f ? rintf(__fdiv_rn(rowbuf[k + e], s)) : 0.0f;
-      r = fminf(fmaxf(r, (float)(-qmax - 1)), (float)qmax);
-      c[e] = (int)r;
+      r = fminf(fmaxf(r, (float)(-qmax)), (float)qmax);
+      c[e] = (uint32_t)fabsf(r) | (r < 0.0f ? (BITS == 4 ? 8u : 0x80u) : 0u);
     }
     if (BITS == 4) {
-      Q[(size_t)n * (K / 2) + k / 2] = (uint8_t)((c[0] & 0xF) | ((c[1] & 0xF) << 4));
+      Q[(size_t)n * (K / 2) + k / 2] = (uint8_t)(c[0] | (c[1] << 4));
     } else {
-      *reinterpret_cast<uint16_t*>(Q + (size_t)n * K + k) =
-          (uint16_t)((c[0] & 0xFF) | ((c[1] & 0xFF) << 8));
+      *reinterpret_cast<uint16_t*>(Q + (size_t)n * K + k) = (uint16_t)(c[0] | (c[1] << 8));
     }
   }
 }

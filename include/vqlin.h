@@ -26,9 +26,13 @@
  *     caller, 16-byte aligned.  bf16 tensors are passed as uint16_t bit
  *     patterns.  All matrices are row-major: X [M, K], W [N, K] (nn.Linear
  *     layout), Y [M, N].
- *   - int4 codes are packed two per byte, two's complement, the even
- *     channel k in the low nibble ([rows, K/2] bytes); asymmetric uint4
- *     codes use the same nibble order.  int8 codes are [rows, K] int8.
+ *   - Symmetric codes lie in [-qmax, qmax] (qmax = 7 or 127) and are stored
+ *     sign-magnitude: an int4 code c is the nibble (c < 0) << 3 | |c|, two
+ *     per byte with the even channel k in the low nibble ([rows, K/2]
+ *     bytes); an int8 code is the byte (c < 0) << 7 | |c| ([rows, K]).
+ *     Asymmetric uint4 codes are plain unsigned nibbles in the same order.
+ *     (The pages fix no packing; sign-magnitude codes convert to exact
+ *     tensor-core operands with a few bit operations.)
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on it.  Argument checks happen on the host before any
  *     launch; a call that returns an error has launched nothing.
@@ -80,7 +84,7 @@ vqlin_status vqlin_get_last_device_error(void* stream);
  *   W~ = W . blockdiag(H_b / sqrt(b)) if hadamard_block b in {64, 128}
  *   (computed in float64, rounded once to float32), else W~ = W;
  *   s[n] = max_k |W~[n,k]| / qmax  (float32, qmax = 7 or 127);
- *   q = clamp(rint(W~ / s), -qmax-1, qmax), round half to even; a zero row
+ *   q = clamp(rint(W~ / s), -qmax, qmax), round half to even; a zero row
  *   gives s = 0 and codes 0.
  *   q_out: int4 [N, K/2] bytes or int8 [N, K]; scale_out: float [N];
  *   zero_out must be NULL.
@@ -107,7 +111,7 @@ vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bit
  *        b = hadamard_block in {0, 64, 128}, 0 = no rotation);
  *   dynamic (static_scale == NULL): s[m] = max_k |x~[m,k]| / qmax;
  *   static: s[m] = *static_scale (ONE device float, > 0, finite);
- *   q = clamp(rint(x~ / s), -qmax-1, qmax), round half to even; s = 0 gives
+ *   q = clamp(rint(x~ / s), -qmax, qmax), round half to even; s = 0 gives
  *   codes 0.
  * X: bf16 [M, K]; q_out: int4 [M, K/2] bytes (bits 4) or int8 [M, K] (bits 8);
  * scale_out: float [M] (filled with the static scale in static mode).
@@ -122,15 +126,18 @@ vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
  * The sum is exact in int32; the epilogue is float32 in that order, rounded
  * half to even to bf16.  (FoldQuantVLA abstract: native integer execution.)
  * xq: int4 [M, K/2]; sx: float [M]; wq: int4 [N, K/2]; sw: float [N];
- * bias: bf16 [N] or NULL; Y: bf16 [M, N].  Requires K % 128 == 0.
+ * bias: bf16 [N] or NULL; Y: bf16 [M, N].  Requires K % 128 == 0 and
+ * K <= 65536.  Runs on the tcgen05 tensor cores (int4 codes as exact e4m3
+ * operands); K may be split over a thread-block cluster, reduced on chip.
  */
 vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t* wq,
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);
 
-/* W8A8 projection: as vqlin_linear_w4a4 with int8 codes xq [M, K], wq [N, K].
- * Requires K % 64 == 0. */
-vqlin_status vqlin_linear_w8a8(const int8_t* xq, const float* sx, const int8_t* wq,
+/* W8A8 projection: as vqlin_linear_w4a4 with int8 codes xq [M, K], wq [N, K]
+ * (exact f16 operands; at most 1024 channels per float32 partial sum, which
+ * bounds it below 2^24).  Requires K % 64 == 0 and K <= 16384. */
+vqlin_status vqlin_linear_w8a8(const uint8_t* xq, const float* sx, const uint8_t* wq,
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);
 
@@ -161,6 +168,18 @@ vqlin_status vqlin_linear_bf16_ref(const uint16_t* X, const uint16_t* W, const u
  */
 vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int32_t* acc,
                                   int M, int N, int K, void* stream);
+
+/*
+ * Test entry point of failure detection: launches the GEMM of
+ * vqlin_debug_gemm_s32 with its tile producer withholding every load, so
+ * that the consumers' bounded waits run out after limit_ns nanoseconds
+ * (0 < limit_ns <= 2e9).  Nothing is left in flight; the kernel records
+ * VQLIN_ERR_TIMEOUT in the device status word, frees its tensor memory and
+ * returns.  The call itself returns VQLIN_OK once launched; the error is
+ * read with vqlin_get_last_device_error().  acc [M, N] is not written.
+ */
+vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const void* wq, int32_t* acc,
+                                             int M, int N, int K, uint64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

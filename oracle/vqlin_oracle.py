@@ -30,7 +30,8 @@ The readings taken here (each a plain textbook choice):
   R1 Sylvester H_b, scaled 1/sqrt(b), b in {64, 128}; blocks are consecutive
      channel ranges [j*b, (j+1)*b).
   R3 symmetric scale = absmax / qmax (qmax = 7 or 127), codes clamped to
-     [-qmax-1, qmax].
+     the symmetric range [-qmax, qmax] (absmax scaling never leaves it; a
+     static scale can, and then clamps to +-qmax).
   R4 round half to even everywhere; x / s is an IEEE float32 division; the
      decision that produces a code is taken in float32 (the kernel's
      precision) from the float32 rounding of the exact rotated value.
@@ -41,8 +42,11 @@ The readings taken here (each a plain textbook choice):
   R7 per-channel and per-token scales are float32.
   R13 final outputs are rounded once to bf16, round half to even.
 
-Packing: int4 codes are two's complement nibbles, two per byte, the even
-channel in the low nibble; asymmetric uint4 codes use the same order.
+Packing (a format of this library; the pages fix none): symmetric codes are
+sign-magnitude -- an int4 code c is the nibble (c < 0) << 3 | |c|, two per
+byte with the even channel in the low nibble; an int8 code is the byte
+(c < 0) << 7 | |c|.  Asymmetric uint4 codes are plain unsigned nibbles in the
+same order.
 """
 from __future__ import annotations
 
@@ -139,7 +143,7 @@ def qmax_of(bits: int) -> int:
 def rtn_symmetric_rows(V32, bits: int):
     """Per-row symmetric RTN of float32 values.
 
-    s = absmax / qmax (float32 division);  q = clamp(rint(v / s), -qmax-1, qmax).
+    s = absmax / qmax (float32 division);  q = clamp(rint(v / s), -qmax, qmax).
     A row whose absmax is 0 gets s = 0 and all codes 0 (R5).
     """
     V32 = np.asarray(V32, dtype=np.float32)
@@ -148,19 +152,19 @@ def rtn_symmetric_rows(V32, bits: int):
     s = (absmax / np.float32(qmax)).astype(np.float32)
     safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
     q = np.rint(V32 / safe[:, None])
-    q = np.clip(q, -qmax - 1, qmax)
+    q = np.clip(q, -qmax, qmax)
     q = np.where(s[:, None] > 0, q, 0.0)
     return q.astype(np.int8), s
 
 
 def rtn_static(V32, bits: int, scale: float):
-    """Quantize with a given float32 scale: clamp(rint(v / s), -qmax-1, qmax)."""
+    """Quantize with a given float32 scale: clamp(rint(v / s), -qmax, qmax)."""
     qmax = qmax_of(bits)
     s = np.float32(scale)
     if not s > 0:
         return np.zeros(np.shape(V32), dtype=np.int8)
     q = np.rint(np.asarray(V32, dtype=np.float32) / s)
-    return np.clip(q, -qmax - 1, qmax).astype(np.int8)
+    return np.clip(q, -qmax, qmax).astype(np.int8)
 
 
 def rtn_asymmetric_groups(V32, group_size: int):
@@ -241,19 +245,48 @@ def rotated_f64(X_bits, hadamard_block: int) -> np.ndarray:
 
 
 def pack_int4(codes) -> np.ndarray:
-    """[R, K] codes in [-8, 15] -> [R, K/2] bytes; even channel in the low nibble."""
-    c = np.asarray(codes).astype(np.int64) & 0xF
+    """[R, K] int4 codes in [-7, 7] -> [R, K/2] sign-magnitude bytes.
+
+    Nibble of code c: (c < 0) << 3 | |c|; the even channel is the low nibble.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    if np.any(np.abs(c) > 7):
+        raise ValueError("int4 codes must lie in [-7, 7]")
+    nib = np.where(c < 0, 8, 0) | np.abs(c)
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+
+
+def pack_uint4(codes) -> np.ndarray:
+    """[R, K] unsigned codes in [0, 15] -> [R, K/2] bytes, even channel low."""
+    c = np.asarray(codes).astype(np.int64)
+    if np.any((c < 0) | (c > 15)):
+        raise ValueError("uint4 codes must lie in [0, 15]")
     return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
 
 
 def unpack_int4(packed, signed: bool) -> np.ndarray:
+    """Inverse of pack_int4 (signed) or pack_uint4 (unsigned)."""
     p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
     lo, hi = p & 0xF, p >> 4
     out = np.empty((p.shape[0], p.shape[1] * 2), dtype=np.int64)
     out[:, 0::2], out[:, 1::2] = lo, hi
     if signed:
-        out = np.where(out >= 8, out - 16, out)
+        out = np.where(out & 8, -(out & 7), out & 7)
     return out.astype(np.int8 if signed else np.uint8)
+
+
+def pack_int8(codes) -> np.ndarray:
+    """[R, K] int8 codes in [-127, 127] -> [R, K] sign-magnitude bytes."""
+    c = np.asarray(codes).astype(np.int64)
+    if np.any(np.abs(c) > 127):
+        raise ValueError("int8 codes must lie in [-127, 127]")
+    return (np.where(c < 0, 0x80, 0) | np.abs(c)).astype(np.uint8)
+
+
+def unpack_int8(packed) -> np.ndarray:
+    """Inverse of pack_int8."""
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    return np.where(p & 0x80, -(p & 0x7F), p & 0x7F).astype(np.int8)
 
 
 # ----------------------------------------------------------------------------

@@ -57,8 +57,12 @@ def rel_fro(a_bits, b_bits):
 
 
 def unpack_codes(q, bits):
-    q = q.cpu().numpy()
-    return o.unpack_int4(q, signed=True) if bits == 4 else q.astype(np.int8)
+    q = q.cpu().numpy().view(np.uint8)
+    return o.unpack_int4(q, signed=True) if bits == 4 else o.unpack_int8(q)
+
+
+def pack_codes(c, bits):
+    return torch.from_numpy(o.pack_int4(c) if bits == 4 else o.pack_int8(c)).to(DEV)
 
 
 def check_act_codes(q_gpu, s_gpu, Xb, bits, hb, static_scale=None):
@@ -110,7 +114,7 @@ def test_act_quant_dynamic(bits, case):
     Xb = activations(M, K, dist=dist, n_outliers=nout, outlier_scale=sc, seed=7, tags=("act", bits))
     X = to_dev_bf16(Xb)
     shape = (M, K // 2) if bits == 4 else (M, K)
-    qg = Guarded(shape, torch.uint8 if bits == 4 else torch.int8)
+    qg = Guarded(shape, torch.uint8)
     sg = Guarded((M,), torch.float32)
     vq.act_hadamard_quant(X, bits, hb, q_out=qg.t, scale_out=sg.t)
     qg.check()
@@ -130,7 +134,8 @@ def test_act_quant_static_scale_clamps(bits):
     check_act_codes(q, sx, Xb, bits, hb, static_scale=s)
     codes = unpack_codes(q, bits)
     qmax = 7 if bits == 4 else 127
-    assert codes.min() == -qmax - 1 or codes.max() == qmax
+    assert codes.min() == -qmax or codes.max() == qmax
+    assert codes.min() >= -qmax
 
 
 @pytest.mark.parametrize("bits", [4, 8])
@@ -196,19 +201,21 @@ def test_weight_quant_asymmetric_bit_exact(group, NK):
 # ------------------------------------------------------------ integer GEMM
 
 GEMM_SHAPES = [(1, 8, 256), (16, 256, 256), (17, 200, 384), (50, 1024, 1024), (129, 257, 512),
-               (128, 128, 2048), (816, 256, 2048), (64, 4096, 128), (3, 11008, 256)]
+               (128, 128, 2048), (816, 256, 2048), (64, 4096, 128), (3, 11008, 256),
+               (50, 1024, 4096), (257, 136, 1024), (512, 384, 2048), (64, 256, 16384),
+               (816, 2560, 2048), (33, 1000, 11008)]
 
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("shape", GEMM_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_int_gemm_bit_exact(bits, shape):
     M, N, K = shape
-    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
-    xq = random_codes((M, K), lo, hi, seed=1, tags=("x", bits))
-    wq = random_codes((N, K), lo, hi, seed=2, tags=("w", bits))
-    pack = o.pack_int4 if bits == 4 else (lambda c: c)
-    xd = torch.from_numpy(pack(xq)).to(DEV)
-    wd = torch.from_numpy(pack(wq)).to(DEV)
+    if bits == 8 and K > 16384:
+        pytest.skip("int8 GEMM supports K <= 16384")
+    qmax = 7 if bits == 4 else 127
+    xq = random_codes((M, K), -qmax, qmax, seed=1, tags=("x", bits))
+    wq = random_codes((N, K), -qmax, qmax, seed=2, tags=("w", bits))
+    xd, wd = pack_codes(xq, bits), pack_codes(wq, bits)
     acc = Guarded((M, N), torch.int32)
     vq.debug_gemm_s32(bits, xd, wd, K, out=acc.t)
     acc.check()
@@ -218,13 +225,30 @@ def test_int_gemm_bit_exact(bits, shape):
 @pytest.mark.parametrize("bits", [4, 8])
 def test_int_gemm_extremes(bits):
     M, N, K = 4, 16, 16384
-    v = -8 if bits == 4 else -128
-    xq = np.full((M, K), v, np.int8)
-    wq = np.full((N, K), v, np.int8)
-    wq[1::2, ::2] = 7 if bits == 4 else 127   # large partial sums that cancel late
-    pack = o.pack_int4 if bits == 4 else (lambda c: c)
-    acc = vq.debug_gemm_s32(bits, torch.from_numpy(pack(xq)).to(DEV),
-                            torch.from_numpy(pack(wq)).to(DEV), K)
+    qmax = 7 if bits == 4 else 127
+    xq = np.full((M, K), -qmax, np.int8)
+    wq = np.full((N, K), -qmax, np.int8)
+    wq[1::2, ::2] = qmax                       # large partial sums that cancel late
+    wq[2, K // 2:] = 1                         # a large sum, then small additions
+    acc = vq.debug_gemm_s32(bits, pack_codes(xq, bits), pack_codes(wq, bits), K)
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_int_gemm_bounded_wait_reports_timeout(bits):
+    # the producer withholds every tile load: the consumers' waits run out
+    # (10 ms), the kernel records a timeout and exits; the context stays usable
+    M, N, K = 16, 128, 1024
+    qmax = 7 if bits == 4 else 127
+    xq = random_codes((M, K), -qmax, qmax, seed=5)
+    wq = random_codes((N, K), -qmax, qmax, seed=6)
+    xd, wd = pack_codes(xq, bits), pack_codes(wq, bits)
+    vq.get_last_device_error()
+    vq.debug_gemm_withheld_loads(bits, xd, wd, K, limit_ns=10_000_000)
+    with pytest.raises(vq.VqlinError, match="TIMEOUT"):
+        vq.get_last_device_error()
+    vq.get_last_device_error()   # the status word was cleared
+    acc = vq.debug_gemm_s32(bits, xd, wd, K)
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
 
 
@@ -273,10 +297,9 @@ def test_linear_epilogue_with_oracle_codes(bits):
     Wb = weights(N, K, seed=32)
     bias = weights(1, N, std=0.5, seed=33)[0]
     ref = o.linear_quantized(Xb, Wb, bits, 128, bias_bits=bias)
-    pack = o.pack_int4 if bits == 4 else (lambda c: c)
     fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
-    y = fn(torch.from_numpy(pack(ref["xq"])).to(DEV), torch.from_numpy(ref["sx"]).to(DEV),
-           torch.from_numpy(pack(ref["wq"])).to(DEV), torch.from_numpy(ref["sw"]).to(DEV),
+    y = fn(pack_codes(ref["xq"], bits), torch.from_numpy(ref["sx"]).to(DEV),
+           pack_codes(ref["wq"], bits), torch.from_numpy(ref["sw"]).to(DEV),
            to_dev_bf16(bias))
     yb = bf16_bits(y).astype(np.int64)
     ulp = np.abs(yb - ref["y"].astype(np.int64))

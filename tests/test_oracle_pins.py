@@ -113,7 +113,7 @@ def test_rtn_symmetric_invariants(bits):
     qmax = 7 if bits == 4 else 127
     v = o.bf16_to_f64(weights(64, 256, spike_frac=0.01, spike_scale=10, seed=9)).astype(np.float32)
     q, s = o.rtn_symmetric_rows(v, bits)
-    assert q.min() >= -qmax - 1 and q.max() <= qmax
+    assert q.min() >= -qmax and q.max() <= qmax
     err = np.abs(v.astype(np.float64) - q.astype(np.float64) * s[:, None].astype(np.float64))
     # half a step, plus the rounding of the float32 quotient v / s (R4)
     assert np.all(err <= s[:, None].astype(np.float64) / 2 + np.abs(v) * 2.0 ** -23)
@@ -125,9 +125,10 @@ def test_rtn_symmetric_invariants(bits):
 def test_rtn_static_clamps_beyond_range():
     v = np.array([[0.5, -0.5, 100.0, -100.0, 6.9, -7.6, 2.5]], dtype=np.float32)
     q = o.rtn_static(v, 4, 1.0)
-    assert q[0].tolist() == [0, 0, 7, -8, 7, -8, 2]
+    # symmetric range [-qmax, qmax]: -100 and -7.6 clamp to -7, not to -8
+    assert q[0].tolist() == [0, 0, 7, -7, 7, -7, 2]
     q8 = o.rtn_static(v, 8, 0.5)
-    assert q8[0].tolist() == [1, -1, 127, -128, 14, -15, 5]
+    assert q8[0].tolist() == [1, -1, 127, -127, 14, -15, 5]
 
 
 def test_rtn_asymmetric_hand_cases():
@@ -208,7 +209,7 @@ def _gemm_bruteforce_kouter(xq, wq):
 
 @pytest.mark.parametrize("bits", [4, 8])
 def test_int_gemm_bruteforce(bits):
-    lo, hi = (-8, 7) if bits == 4 else (-128, 127)
+    lo, hi = (-7, 7) if bits == 4 else (-127, 127)
     xq = random_codes((5, 96), lo, hi, seed=1)
     wq = random_codes((7, 96), lo, hi, seed=2)
     ref = _gemm_bruteforce(xq, wq)
@@ -218,21 +219,36 @@ def test_int_gemm_bruteforce(bits):
 
 def test_int_gemm_adversarial_extremes():
     K = 16384
-    x = np.full((2, K), -8, np.int8)
-    w = np.full((3, K), -8, np.int8)
-    assert np.all(o.int_gemm(x, w) == 64 * K)
-    x8 = np.full((2, K), -128, np.int8)
-    w8 = np.full((2, K), -128, np.int8)
-    w8[1, ::2] = 127
+    x = np.full((2, K), -7, np.int8)
+    w = np.full((3, K), -7, np.int8)
+    assert np.all(o.int_gemm(x, w) == 49 * K)
+    x8 = np.full((2, K), -127, np.int8)
+    w8 = np.full((2, K), -127, np.int8)
+    w8[1, ::2] = 126
     acc = o.int_gemm(x8, w8)
-    assert acc[0, 0] == 16384 * K and acc[0, 1] == (16384 - 128 * 127) * K // 2
+    assert acc[0, 0] == 16129 * K and acc[0, 1] == (16129 - 127 * 126) * K // 2
 
 
 def test_pack_int4_format():
-    codes = np.array([[1, -1, -8, 7, 0, 5]], dtype=np.int8)
+    # sign-magnitude nibbles (c < 0) << 3 | |c|, even channel in the low nibble
+    codes = np.array([[1, -1, -7, 7, 0, 5]], dtype=np.int8)
     p = o.pack_int4(codes)
-    assert p[0].tolist() == [0xF1, 0x78, 0x50]
+    assert p[0].tolist() == [0x91, 0x7F, 0x50]
     assert np.array_equal(o.unpack_int4(p, True), codes)
+    with pytest.raises(ValueError):
+        o.pack_int4(np.array([[-8, 0]], dtype=np.int8))
+    u = np.array([[0, 15, 8, 1]], dtype=np.uint8)
+    assert o.pack_uint4(u)[0].tolist() == [0xF0, 0x18]
+    assert np.array_equal(o.unpack_int4(o.pack_uint4(u), False), u)
+
+
+def test_pack_int8_format():
+    codes = np.array([[1, -1, 127, -127, 0, -64]], dtype=np.int8)
+    p = o.pack_int8(codes)
+    assert p[0].tolist() == [0x01, 0x81, 0x7F, 0xFF, 0x00, 0xC0]
+    assert np.array_equal(o.unpack_int8(p), codes)
+    with pytest.raises(ValueError):
+        o.pack_int8(np.array([[-128]], dtype=np.int16))
 
 
 # ---------------------------------------------------------------- epilogue / W4A16 / bf16
@@ -318,4 +334,4 @@ def test_static_scale_calibration_is_max_of_dynamic_scales():
     dyn = max(o.act_hadamard_quant(d, 4, 64)[1].max() for d in draws)
     assert s == dyn
     q, sx = o.act_hadamard_quant(draws[0], 4, 64, static_scale=s)
-    assert np.all(sx == s) and q.min() >= -8 and q.max() <= 7
+    assert np.all(sx == s) and q.min() >= -7 and q.max() <= 7
