@@ -110,6 +110,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_sx[256], s_sw[kTileN], s_bias[kTileN];
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int bt = a.bt;
@@ -125,6 +126,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   uint64_t* op_full = bars + 2 * R;
   uint64_t* op_empty = bars + 2 * R + kOpStages;
   uint64_t* acc_full = bars + 2 * R + 2 * kOpStages;
+  uint64_t* scl_ready = acc_full + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z;
@@ -146,6 +148,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       mbar_init(&op_empty[i], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(scl_ready, 31);
     mbar_init_fence();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -157,6 +160,20 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
+    // lanes 1..31 stage the epilogue's per-token and per-channel scales and the
+    // bias (float) while lane 0 produces; the epilogue reads them after a
+    // CTA-wide or cluster-wide barrier
+    if (lane > 0) {
+      if (a.acc == nullptr) {
+        for (int i = lane - 1; i < bt; i += 31) s_sx[i] = m0 + i < a.M ? __ldg(a.sx + m0 + i) : 0.0f;
+        for (int i = lane - 1; i < kTileN; i += 31) {
+          const bool in = n0 + i < a.N;
+          s_sw[i] = in ? __ldg(a.sw + n0 + i) : 0.0f;
+          s_bias[i] = in && a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n0 + i) << 16) : 0.0f;
+        }
+      }
+      mbar_arrive(scl_ready);
+    }
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = 0;
@@ -231,58 +248,113 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   }
 
   // ---------------------------------------------------------------- epilogue
-  // The int32 partial tile [128 channels][bt tokens] (row stride bt + 1 words)
-  // overlays the operand and raw rings, which are idle once acc_full completes.
   __syncwarp();  // the single-thread roles rejoin their warps
-  int32_t* part = reinterpret_cast<int32_t*>(base);
-  const int ldp = bt + 1;
+  const float unit = BITS == 4 ? 262144.0f : 281474976710656.0f;  // 2^18, 2^48: accumulator -> integer
+  const bool raw_out = a.acc != nullptr;
+  bool go = false;
   if (warp >= 2) {
-    const bool ok = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, nullptr);
+    const bool ok = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, nullptr) &&
+                    mbar_wait_bounded(scl_ready, 0, a.wait_limit_ns, nullptr);
     if (!ok) record_timeout(a.status, abort);
     tc_fence_after();
     // warp-uniform decision: the tensor-memory loads below are warp-collective
-    if (__all_sync(0xffffffffu, ok && !*abort)) {
-      const int q = warp & 3;              // tensor-memory lane quadrant of this warp
-      const int row = q * 32 + lane;       // output channel inside the tile
-      const float unit = BITS == 4 ? 262144.0f : 281474976710656.0f;  // 2^18, 2^48
+    go = __all_sync(0xffffffffu, ok && !*abort);
+  }
+  const int q = warp & 3;          // tensor-memory lane quadrant of this warp
+  const int row = q * 32 + lane;   // output channel inside the tile (warps 2..5)
+
+  if (S == 1) {
+    // straight from tensor memory to global memory: thread = channel, 16
+    // tokens per load; for each token the warp writes 32 consecutive channels
+    if (warp >= 2 && go) {
+      const int n = n0 + row;
+      const float sw_n = s_sw[row], b_n = s_bias[row];
+      for (int c0 = 0; c0 < bt; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld_wait();
+        if (n < a.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < a.M) {
+              const int32_t acc = __float2int_rn(__uint_as_float(v[j]) * unit);
+              if (raw_out) {
+                a.acc[(size_t)m * a.N + n] = acc;
+              } else {
+                const float y = __fadd_rn(__fmul_rn(__fmul_rn((float)acc, s_sx[c0 + j]), sw_n), b_n);
+                a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(y);
+              }
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    // split K: int32 partial tile part[token][channel] in this CTA's shared
+    // memory (it overlays the idle rings); after a cluster barrier, CTA r of
+    // the cluster sums channels [r0, r0 + rows_per) over all S partials with
+    // 16-byte DSMEM loads and writes them out.
+    int32_t* part = reinterpret_cast<int32_t*>(base);
+    if (warp >= 2 && go) {
       for (int c0 = 0; c0 < bt; c0 += 16) {
         uint32_t v[16];
         tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          part[row * ldp + c0 + j] = __float2int_rn(__uint_as_float(v[j]) * unit);
+        for (int j = 0; j < 16; ++j) part[(c0 + j) * kTileN + row] = __float2int_rn(__uint_as_float(v[j]) * unit);
       }
     }
-  }
-  tc_fence_before();
-  cluster_sync_all();
-
-  if (!*abort) {
-    const int rows_per = (kTileN + S - 1) / S;
-    const int r0 = (int)rank * rows_per;
-    const int r1 = min(kTileN, r0 + rows_per);
-    const int nr = r1 - r0;
-    if (nr > 0) {
+    tc_fence_before();
+    cluster_sync_all();
+    if (!*abort) {
+      const int rows_per = ((kTileN + S - 1) / S + 3) & ~3;
+      const int r0 = (int)rank * rows_per;
+      const int nq = (min(kTileN, r0 + rows_per) - r0) / 4;  // 4-channel groups owned here
       const uint32_t part_s = smem_addr(part);
-      for (int idx = tid; idx < nr * bt; idx += kThreads) {
-        const int rr = r0 + idx % nr, col = idx / nr;
-        const int n = n0 + rr, m = m0 + col;
-        if (n >= a.N || m >= a.M) continue;
-        const uint32_t off = (uint32_t)(rr * ldp + col) * 4u;
-        int32_t sum = 0;
-        for (int c = 0; c < S; ++c) sum += ld_shared_cluster_s32(mapa_shared(part_s + off, (uint32_t)c));
-        if (a.acc != nullptr) {
-          a.acc[(size_t)m * a.N + n] = sum;
+      const bool vec = (a.N & 3) == 0;
+      for (int idx = tid; idx < nq * bt; idx += kThreads) {
+        const int rr = r0 + 4 * (idx % nq), col = idx / nq;
+        const int m = m0 + col, n = n0 + rr;
+        if (m >= a.M || n >= a.N) continue;
+        const uint32_t off = (uint32_t)(col * kTileN + rr) * 4u;
+        int4 pv[kMaxSplit];
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c)
+          if (c < S) pv[c] = ld_shared_cluster_v4(mapa_shared(part_s + off, (uint32_t)c));
+        int32_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c)
+          if (c < S) {
+            acc[0] += pv[c].x; acc[1] += pv[c].y; acc[2] += pv[c].z; acc[3] += pv[c].w;
+          }
+        if (raw_out) {
+          int32_t* dst = a.acc + (size_t)m * a.N + n;
+          if (vec) {
+            *reinterpret_cast<int4*>(dst) = make_int4(acc[0], acc[1], acc[2], acc[3]);
+          } else {
+            for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = acc[e];
+          }
         } else {
-          float y = __fmul_rn(__fmul_rn((float)sum, __ldg(a.sx + m)), __ldg(a.sw + n));
-          if (a.bias != nullptr) y = __fadd_rn(y, __uint_as_float((uint32_t)__ldg(a.bias + n) << 16));
-          a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(y);
+          uint16_t y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            y[e] = f32_to_bf16_rn(__fadd_rn(__fmul_rn(__fmul_rn((float)acc[e], s_sx[col]), s_sw[rr + e]),
+                                            s_bias[rr + e]));
+          uint16_t* dst = a.Y + (size_t)m * a.N + n;
+          if (vec) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2((uint32_t)y[0] | ((uint32_t)y[1] << 16),
+                                                        (uint32_t)y[2] | ((uint32_t)y[3] << 16));
+          } else {
+            for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = y[e];
+          }
         }
       }
     }
+    cluster_sync_all();  // peers have finished reading this CTA's shared memory
   }
-  cluster_sync_all();  // peers have finished reading this CTA's shared memory
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -318,11 +390,11 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, int rows, int row_bytes, int bo
 }
 
 // 227 KB opt-in per CTA, less room for the kernel's static shared memory
-constexpr int kMaxSmem = 232448 - 1024;
+constexpr int kMaxSmem = 232448 - 4096;
 
 size_t smem_bytes(int bt, int raw_stages) {
   const size_t rows = kTileN + bt;
-  return 1024 + kOpStages * rows * kOpRow + raw_stages * rows * kRawRow + (2 * raw_stages + 2 * kOpStages + 1) * 8;
+  return 1024 + kOpStages * rows * kOpRow + raw_stages * rows * kRawRow + (2 * raw_stages + 2 * kOpStages + 2) * 8;
 }
 
 template <int BITS>
