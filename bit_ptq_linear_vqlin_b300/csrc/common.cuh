@@ -1,6 +1,7 @@
 // Shared device helpers and internal launcher declarations of libvqlin.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -22,6 +23,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline unsigned ceil_div(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
 
+// 2-D tiled TMA descriptor: a [rows, inner] matrix of `dtype` elements whose
+// rows are row_bytes apart, copied in boxes of box_inner x box_rows elements;
+// out-of-range elements read as zero.  False if the driver rejects it
+// (tmap.cu).
+bool tmap_encoder_available();
+bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                    uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                    CUtensorMapSwizzle swizzle);
+
 // Launchers (defined in the kernel files).  They assume validated arguments.
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
                              const float* static_scale, void* q, float* s, cudaStream_t st);
@@ -39,9 +49,14 @@ vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const vo
 vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, int32_t* acc,
                                       int M, int N, int K, int* status, uint64_t limit_ns,
                                       cudaStream_t st);
-cudaError_t launch_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
-                         const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
-                         int M, int N, int K, int* status, cudaStream_t st);
+// W4A16: CUDA-core GEMV (M <= 4) and tcgen05 dequant-GEMM (any M).
+cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
+                              const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
+                              int M, int N, int K, int* status, cudaStream_t st);
+vqlin_status launch_w4a16_tc(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
+                             const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
+                             int M, int N, int K, int* status, cudaStream_t st);
+constexpr int kW4a16GemvMaxM = 4;
 
 // Largest K each kernel supports (host-side shape checks).
 constexpr int kActQuantMaxK = 65536;

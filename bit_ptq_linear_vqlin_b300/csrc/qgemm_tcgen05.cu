@@ -35,9 +35,6 @@
 //     is deterministic.
 // Every wait is bounded in time; a wait that runs out records
 // VQLIN_ERR_TIMEOUT in the device status word and the CTA winds down.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "common.cuh"
@@ -360,36 +357,13 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // Tensor map of a [rows, row_bytes] uint8 matrix, box = 64 bytes x box_rows,
 // no swizzle; out-of-range rows read as zero.
 bool make_tmap(CUtensorMap* tm, const void* ptr, int rows, int row_bytes, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)kRawRow, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return vqlin::encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, (uint64_t)row_bytes, (uint64_t)rows,
+                               (uint64_t)row_bytes, kRawRow, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// 227 KB opt-in per CTA, less room for the kernel's static shared memory
 constexpr int kMaxSmem = 232448 - 4096;
 
 size_t smem_bytes(int bt, int raw_stages) {
@@ -435,7 +409,8 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   while ((int)cols < bt) cols <<= 1;
 
   CUtensorMap tmW, tmX;
-  if (!encode_fn()) return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cuTensorMapEncodeTiled is unavailable");
+  if (!vqlin::tmap_encoder_available())
+    return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cuTensorMapEncodeTiled is unavailable");
   if (!make_tmap(&tmW, wq, N, row_bytes, kTileN) || !make_tmap(&tmX, xq, M, row_bytes, bt))
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
 

@@ -257,9 +257,11 @@ vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint
   REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(scales); REQUIRE_ALIGNED(zeros); REQUIRE_ALIGNED(Y);
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
-  return vqlin::check_launch(vqlin::launch_w4a16(X, wq, scales, zeros, group_size, bias, Y, M, N, K, status,
-                                                 static_cast<cudaStream_t>(stream)),
-                             "linear_w4a16");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M <= vqlin::kW4a16GemvMaxM)
+    return vqlin::check_launch(vqlin::launch_w4a16_gemv(X, wq, scales, zeros, group_size, bias, Y, M, N, K, status, st),
+                               "linear_w4a16");
+  return vqlin::launch_w4a16_tc(X, wq, scales, zeros, group_size, bias, Y, M, N, K, status, st);
 }
 
 vqlin_status vqlin_linear_bf16_ref(const uint16_t* X, const uint16_t* W, const uint16_t* bias, uint16_t* Y,

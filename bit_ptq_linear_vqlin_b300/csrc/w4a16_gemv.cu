@@ -1,4 +1,5 @@
-// Weight-only int4 projection (W4A16), CUDA-core GEMV path for few tokens.
+// Weight-only int4 projection (W4A16), CUDA-core GEMV path for at most 4
+// tokens (the tensor-core kernel in w4a16_tcgen05.cu serves larger M).
 //
 //   Wdq[n, k] = (q[n, k] - z[n, k/g]) * s[n, k/g]     (exact in float32)
 //   Y[m, n]   = bf16(sum_k X[m, k] * Wdq[n, k] + bias[n]), float32 accumulation
@@ -60,7 +61,8 @@ w4a16_gemv_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ Wq
       const float z = __uint_as_float((uint32_t)__ldg(Zg + (size_t)n * G + g) << 16);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float q = (float)((w >> (4 * e)) & 0xFu);
+        // channel 2i in bits [4i, 4i+4), channel 2i+1 in bits [16+4i, 16+4i+4)
+        const float q = (float)((w >> ((e & 1) * 16 + 4 * (e >> 1))) & 0xFu);
         const float wd = (q - z) * s;  // exact: 5-bit integer times a bf16 value
 #pragma unroll
         for (int t = 0; t < TOK; ++t) acc[r][t] = fmaf(x[t][e], wd, acc[r][t]);
@@ -94,7 +96,7 @@ w4a16_gemv_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ Wq
 
 namespace vqlin {
 
-cudaError_t launch_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
+cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
                          const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
                          int M, int N, int K, int* /*status*/, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;

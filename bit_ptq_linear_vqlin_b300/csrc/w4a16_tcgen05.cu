@@ -1,0 +1,427 @@
+// Weight-only int4 projection (W4A16) on the tcgen05 tensor cores.
+//
+//   Y[m, n] = bf16( sum_g s[n,g] * sum_{k in g} X[m,k] * (q[n,k] - z[n,g]) + bias[n] )
+//
+// which is sum_k X[m,k] * Wdq[n,k] with Wdq = (q - z) * s regrouped: the
+// integer (q - z) is an exact bf16 operand, each group's partial sum is kept
+// apart in tensor memory, and its scale is applied in float32 when it is
+// drained.  No weight is rounded to bf16, so the only rounding besides the
+// final one is float32 accumulation.
+//
+// Method: "LoopQ" abstract (the action expert is memory-bound, 63% of GPU
+// time; weight bytes dominate), with group-wise asymmetric RTN weights.
+//
+// Packed weights: per 8 channels one 32-bit word, channel 2i in bits
+// [4i, 4i+4) and channel 2i+1 in bits [16+4i, 16+4i+4), so one shift and one
+// mask give the codes of two consecutive channels in the two halves of a
+// word; OR with 0x4300 makes each half the bf16 value 128 + q, and a bf16x2
+// subtraction of 128 + z leaves q - z exactly.
+//
+// Work decomposition (weights on the MMA's M side):
+//   * one CTA: 128 output channels x BT tokens (BT in {16, 32, 64}) over
+//     a range of whole groups of K; the S CTAs that split K form a cluster;
+//   * warp 0: TMA producer; each stage holds the packed weight tile (32 bytes
+//     of each row per 64-channel k-block) and the activation tile, which TMA
+//     writes directly in the 128-byte swizzled MMA layout;
+//   * warps 2..5: unpack the weight tile into bf16 (q - z) operand rows;
+//   * warp 1: tensor memory and the MMAs (kind::f16, bf16 x bf16 -> f32), one
+//     accumulator per group, double-buffered;
+//   * warps 6..9: drain each group's accumulator, y += s[n,g] * partial, in
+//     registers; then the bias epilogue, with split K summed over the
+//     cluster's shared memory in a fixed order (deterministic).
+// Every wait is bounded in time (VQLIN_ERR_TIMEOUT in the status word).
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+using namespace vqlin_dev;
+
+constexpr int kTileN = 128;
+constexpr int kKB = 64;           // channels per k-block (one 128-byte bf16 row)
+constexpr int kRawRow = 32;       // packed weight bytes of one row per k-block
+constexpr int kOpRow = 128;
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kUnpackThreads = 128;
+constexpr int kDrainThreads = 128;
+constexpr int kMaxSplit = 16;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+struct W4a16Args {
+  const uint16_t* scales;  // bf16 [N, G]
+  const uint16_t* zeros;   // bf16 [N, G]
+  const uint16_t* bias;    // bf16 [N] or null
+  uint16_t* Y;
+  int* status;
+  int M, N, K, G;          // G = K / group
+  int stages;
+  uint32_t tmem_cols;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, 0, (int)VQLIN_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 8 packed codes (one word) -> 8 bf16 values q - z (16 bytes), channel order.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zz) {
+  uint4 o;
+  o.x = bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zz);
+  o.y = bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zz);
+  o.z = bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zz);
+  o.w = bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zz);
+  return o;
+}
+
+// bf16x2 bit pattern of (128 + z, 128 + z) for the zero point of row n, group g.
+__device__ __forceinline__ uint32_t zero_pair(const W4a16Args& a, int n, int g) {
+  uint32_t z = 0;
+  if (n < a.N) z = (uint32_t)__uint_as_float((uint32_t)__ldg(a.zeros + (size_t)n * a.G + g) << 16);
+  const uint32_t h = 0x4300u + z;
+  return h | (h << 16);
+}
+
+template <int BT, int GROUP>
+__global__ void __launch_bounds__(kThreads, 1)
+w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const W4a16Args a) {
+  constexpr int KB_PER_G = GROUP / kKB;
+  constexpr uint32_t kStageTx = kTileN * kRawRow + BT * kOpRow;
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kStageBytes = kTileN * kOpRow + BT * kOpRow + kTileN * kRawRow;  // opA | opB | rawA
+  const int NS = a.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * kStageBytes);
+  uint64_t* full = bars;              // TMA -> unpack
+  uint64_t* opa = bars + NS;          // unpack -> MMA
+  uint64_t* empty = bars + 2 * NS;    // MMA -> TMA
+  uint64_t* accf = bars + 3 * NS;     // [2] MMA -> drain
+  uint64_t* acce = accf + 2;          // [2] drain -> MMA
+  uint64_t* done = acce + 2;          // every MMA issued has completed
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = (int)gridDim.z;
+  const uint32_t rank = cluster_ctarank();
+  const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * BT;
+  const int g0 = (int)(((long long)rank * a.G) / S);
+  const int g1 = (int)(((long long)(rank + 1) * a.G) / S);
+  const int ng = g1 - g0;
+  const int cnt = ng * KB_PER_G;            // k-blocks of this CTA
+  const int kb0 = g0 * KB_PER_G;
+  volatile int* abort = &s_abort;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&opa[i], kUnpackThreads);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], kDrainThreads);
+    }
+    mbar_init(done, 1);
+    mbar_init_fence();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  float y[BT];
+#pragma unroll
+  for (int c = 0; c < BT; ++c) y[c] = 0.0f;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < cnt; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, a.wait_limit_ns, abort)) {
+          if (!*abort) record_timeout(a.status, abort);
+          break;
+        }
+        uint8_t* st = base + (size_t)s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageTx);
+        tma_load_2d(st + kTileN * kOpRow + BT * kOpRow, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
+        tma_load_2d(st + kTileN * kOpRow, &tmX, (kb0 + i) * kKB, m0, &full[s]);
+        ++issued;
+      }
+      for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+        if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
+          record_timeout(a.status, abort);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
+      bool ok = true;
+      for (int i = 0; i < cnt && ok; ++i) {
+        const int s = i % NS;
+        const int jl = i / KB_PER_G, kin = i % KB_PER_G;  // local group, k-block inside it
+        const uint32_t acc = tmem + (uint32_t)((jl & 1) * BT);
+        if (kin == 0 && jl >= 2 &&
+            !mbar_wait_bounded(&acce[jl & 1], ((jl >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
+          if (!*abort) record_timeout(a.status, abort);
+          break;
+        }
+        if (!mbar_wait_bounded(&opa[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
+          if (!*abort) record_timeout(a.status, abort);
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* st = base + (size_t)s * kStageBytes;
+        const uint64_t da = sdesc_sw128(st), db = sdesc_sw128(st + kTileN * kOpRow);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_f16(acc, da + 2 * j, db + 2 * j, id, (kin | j) != 0);
+        tc_commit(&empty[s]);
+        if (kin == KB_PER_G - 1) tc_commit(&accf[jl & 1]);
+      }
+      (void)ok;
+      tc_commit(done);  // tensor memory is freed only after this completes
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ unpackers
+    // thread t: word c = t % 8 of rows t/8 + 16 i, i = 0..7 (fixed rows, so the
+    // zero points of a group are loaded once per group)
+    const int t = tid - 64, c = t & 7, rbase = t >> 3;
+    uint32_t zz[8];
+    int zg = -1;
+    for (int i = 0; i < cnt; ++i) {
+      const int s = i % NS;
+      const int g = g0 + i / KB_PER_G;
+      if (g != zg) {
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) zz[ii] = zero_pair(a, n0 + rbase + 16 * ii, g);
+        zg = g;
+      }
+      if (!mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
+        if (!*abort) record_timeout(a.status, abort);
+        break;
+      }
+      uint8_t* st = base + (size_t)s * kStageBytes;
+      const uint8_t* raw = st + kTileN * kOpRow + BT * kOpRow;
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const int r = rbase + 16 * ii;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + r * kRawRow + c * 4);
+        *reinterpret_cast<uint4*>(st + r * kOpRow + ((c ^ (r & 7)) << 4)) = dequant_word(w, zz[ii]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&opa[s]);
+    }
+  } else {
+    // ------------------------------------------------- group drains (warps 6..9)
+    const int q = warp & 3, row = q * 32 + lane, n = n0 + row;
+    float sg_next = 0.0f;
+    if (ng > 0 && n < a.N) sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0) << 16);
+    for (int jl = 0; jl < ng; ++jl) {
+      const float sg = sg_next;
+      if (jl + 1 < ng && n < a.N)
+        sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0 + jl + 1) << 16);
+      const bool ok = mbar_wait_bounded(&accf[jl & 1], (jl >> 1) & 1, a.wait_limit_ns, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (!ok && !*abort) record_timeout(a.status, abort);
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BT; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((jl & 1) * BT + c0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[c0 + j] = fmaf(sg, __uint_as_float(v[j]), y[c0 + j]);
+      }
+      tc_fence_before();
+      mbar_arrive(&acce[jl & 1]);
+    }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  __syncwarp();
+  if (S == 1) {
+    if (warp >= 6 && !*abort) {
+      const int row = (warp & 3) * 32 + lane, n = n0 + row;
+      if (n < a.N) {
+        const float b = a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n) << 16) : 0.0f;
+#pragma unroll
+        for (int c = 0; c < BT; ++c)
+          if (m0 + c < a.M) a.Y[(size_t)(m0 + c) * a.N + n] = f32_to_bf16_rn(__fadd_rn(y[c], b));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    // float partial tile part[token][channel] over the idle stage ring
+    float* part = reinterpret_cast<float*>(base);
+    __syncthreads();  // every role is past the ring before it is overwritten
+    if (warp >= 6 && !*abort) {
+      const int row = (warp & 3) * 32 + lane;
+#pragma unroll
+      for (int c = 0; c < BT; ++c) part[c * kTileN + row] = y[c];
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    if (!*abort) {
+      const int rows_per = ((kTileN + S - 1) / S + 3) & ~3;
+      const int r0 = (int)rank * rows_per;
+      const int nq = (min(kTileN, r0 + rows_per) - r0) / 4;
+      const uint32_t part_s = smem_addr(part);
+      const bool vec = (a.N & 3) == 0;
+      for (int idx = tid; idx < nq * BT; idx += kThreads) {
+        const int rr = r0 + 4 * (idx % nq), col = idx / nq;
+        const int m = m0 + col, n = n0 + rr;
+        if (m >= a.M || n >= a.N) continue;
+        const uint32_t off = (uint32_t)(col * kTileN + rr) * 4u;
+        float4 pv[kMaxSplit];
+#pragma unroll
+        for (int cc = 0; cc < kMaxSplit; ++cc)
+          if (cc < S) pv[cc] = ld_shared_cluster_v4f(mapa_shared(part_s + off, (uint32_t)cc));
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int cc = 0; cc < kMaxSplit; ++cc)
+          if (cc < S) {
+            acc[0] += pv[cc].x; acc[1] += pv[cc].y; acc[2] += pv[cc].z; acc[3] += pv[cc].w;
+          }
+        uint16_t yo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float b = (a.bias != nullptr && n + e < a.N) ? __uint_as_float((uint32_t)__ldg(a.bias + n + e) << 16)
+                                                              : 0.0f;
+          yo[e] = f32_to_bf16_rn(__fadd_rn(acc[e], b));
+        }
+        uint16_t* dst = a.Y + (size_t)m * a.N + n;
+        if (vec) {
+          *reinterpret_cast<uint2*>(dst) =
+              make_uint2((uint32_t)yo[0] | ((uint32_t)yo[1] << 16), (uint32_t)yo[2] | ((uint32_t)yo[3] << 16));
+        } else {
+          for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = yo[e];
+        }
+      }
+    }
+    cluster_sync_all();
+  }
+  if (warp == 1) {
+    if (!mbar_wait_bounded(done, 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
+    __syncwarp();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kMaxSmem = 232448 - 4096;
+
+template <int BT>
+constexpr size_t stage_bytes() {
+  return (size_t)kTileN * kOpRow + (size_t)BT * kOpRow + (size_t)kTileN * kRawRow;
+}
+
+template <int BT>
+size_t smem_bytes(int stages) {
+  return 1024 + stages * stage_bytes<BT>() + (3 * stages + 5) * 8;
+}
+
+template <int BT, int GROUP>
+vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z,
+                      const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr_err != cudaSuccess)
+    return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + BT - 1) / BT;
+  const int G = K / GROUP;
+  int S = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
+  S = S > kMaxSplit ? kMaxSplit : S;
+  S = S > G ? G : S;
+  const int per_cta = (G + S - 1) / S * (GROUP / kKB);
+  int NS = 6;
+  while (NS > 2 && smem_bytes<BT>(NS) > (size_t)kMaxSmem) --NS;
+  if (NS > per_cta) NS = per_cta < 2 ? 2 : per_cta;
+  // the float partial tile of the split-K epilogue overlays the stage ring
+  static_assert(2 * stage_bytes<BT>() >= (size_t)BT * kTileN * 4, "partial tile must fit two stages");
+  uint32_t cols = 32;
+  while ((int)cols < 2 * BT) cols <<= 1;
+
+  CUtensorMap tmW, tmX;
+  if (!vqlin::tmap_encoder_available())
+    return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: cuTensorMapEncodeTiled is unavailable");
+  if (!vqlin::encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
+                             kRawRow, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !vqlin::encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
+                             kKB, BT, CU_TENSOR_MAP_SWIZZLE_128B))
+    return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
+
+  W4a16Args a;
+  a.scales = s; a.zeros = z; a.bias = bias; a.Y = Y; a.status = status;
+  a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.wait_limit_ns = kWaitLimitNs;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_m, S);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<BT>(NS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = S;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BT, GROUP>, tmW, tmX, a);
+  if (e != cudaSuccess)
+    return vqlin::fail(VQLIN_ERR_CUDA, "w4a16 launch (grid %d x %d x %d, %zu B smem): %s", tiles_n, tiles_m, S,
+                       cfg.dynamicSmemBytes, cudaGetErrorString(e));
+  return VQLIN_OK;
+}
+
+template <int BT>
+vqlin_status launch_bt(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z, int group,
+                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+  switch (group) {
+    case 64: return launch_t<BT, 64>(X, wq, s, z, bias, Y, M, N, K, status, st);
+    case 128: return launch_t<BT, 128>(X, wq, s, z, bias, Y, M, N, K, status, st);
+    default: return launch_t<BT, 256>(X, wq, s, z, bias, Y, M, N, K, status, st);
+  }
+}
+
+}  // namespace
+
+namespace vqlin {
+
+vqlin_status launch_w4a16_tc(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z, int group,
+                             const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+  if (M == 0 || N == 0) return VQLIN_OK;
+  // token tile: the smallest of 16, 32, 64 that covers M in as few tiles as
+  // possible (the drain warps keep BT float sums per thread in registers)
+  const int tiles = (M + 63) / 64;
+  const int per = (M + tiles - 1) / tiles;
+  if (per <= 16) return launch_bt<16>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
+  if (per <= 32) return launch_bt<32>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
+  return launch_bt<64>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
+}
+
+}  // namespace vqlin

@@ -132,20 +132,27 @@ weight_quant_asym_kernel(const uint16_t* __restrict__ W, int N, int K, uint8_t* 
     Sg[(size_t)n * G + g] = (uint16_t)(__float_as_uint(s) >> 16);   // exact: s is a bf16 value
     Zg[(size_t)n * G + g] = (uint16_t)(__float_as_uint(z) >> 16);   // exact: integer 0..15
   }
-  uint8_t bytes[EPL / 2];
+  // packed layout: per 8 channels one 32-bit word, channel 2i in bits
+  // [4i, 4i+4) and channel 2i+1 in bits [16+4i, 16+4i+4); the lanes sharing a
+  // word OR their nibbles together
+  uint32_t word = 0;
 #pragma unroll
-  for (int e = 0; e < EPL; e += 2) {
-    int c[2];
-#pragma unroll
-    for (int d = 0; d < 2; ++d) {
-      float q = rintf(__fdiv_rn(v[e + d], s)) + z;
-      c[d] = (int)fminf(fmaxf(q, 0.0f), 15.0f);
-    }
-    bytes[e / 2] = (uint8_t)(c[0] | (c[1] << 4));
+  for (int e = 0; e < EPL; ++e) {
+    float qf = rintf(__fdiv_rn(v[e], s)) + z;
+    const uint32_t c = (uint32_t)fminf(fmaxf(qf, 0.0f), 15.0f);
+    const int p = (lane * EPL + e) & 7;  // position inside the word
+    word |= c << ((p & 1) * 16 + 4 * (p >> 1));
   }
-  uint8_t* dst = Q + (size_t)n * (K / 2) + (size_t)g * (group / 2) + lane * (EPL / 2);
+  constexpr int LPW = EPL >= 8 ? 1 : 8 / EPL;  // lanes per word
 #pragma unroll
-  for (int e = 0; e < EPL / 2; ++e) dst[e] = bytes[e];
+  for (int o = 1; o < LPW; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+  if (EPL >= 8) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(Q + (size_t)n * (K / 2) + (size_t)g * (group / 2)) + lane * (EPL / 8);
+    dst[0] = word;
+  } else if ((lane % LPW) == 0) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(Q + (size_t)n * (K / 2) + (size_t)g * (group / 2)) + lane / LPW;
+    *dst = word;
+  }
 }
 
 }  // namespace

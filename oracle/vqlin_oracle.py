@@ -45,8 +45,9 @@ The readings taken here (each a plain textbook choice):
 Packing (a format of this library; the pages fix none): symmetric codes are
 sign-magnitude -- an int4 code c is the nibble (c < 0) << 3 | |c|, two per
 byte with the even channel in the low nibble; an int8 code is the byte
-(c < 0) << 7 | |c|.  Asymmetric uint4 codes are plain unsigned nibbles in the
-same order.
+(c < 0) << 7 | |c|.  Asymmetric uint4 codes (W4A16) are unsigned nibbles,
+eight channels per little-endian 32-bit word: channel 2i in bits [4i, 4i+4),
+channel 2i+1 in bits [16+4i, 16+4i+4).
 """
 from __future__ import annotations
 
@@ -257,15 +258,39 @@ def pack_int4(codes) -> np.ndarray:
 
 
 def pack_uint4(codes) -> np.ndarray:
-    """[R, K] unsigned codes in [0, 15] -> [R, K/2] bytes, even channel low."""
+    """[R, K] asymmetric codes in [0, 15] -> [R, K/2] bytes (W4A16 layout).
+
+    Each run of 8 channels is one little-endian 32-bit word: channel 2i in
+    bits [4i, 4i+4), channel 2i+1 in bits [16+4i, 16+4i+4), i = 0..3.
+    """
     c = np.asarray(codes).astype(np.int64)
     if np.any((c < 0) | (c > 15)):
         raise ValueError("uint4 codes must lie in [0, 15]")
-    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    R, K = c.shape
+    if K % 8:
+        raise ValueError("K must be a multiple of 8")
+    g = c.reshape(R, K // 8, 8)
+    word = np.zeros((R, K // 8), dtype=np.int64)
+    for i in range(4):
+        word |= g[:, :, 2 * i] << (4 * i)
+        word |= g[:, :, 2 * i + 1] << (16 + 4 * i)
+    return word.astype("<u4").view(np.uint8).reshape(R, K // 2)
 
 
-def unpack_int4(packed, signed: bool) -> np.ndarray:
-    """Inverse of pack_int4 (signed) or pack_uint4 (unsigned)."""
+def unpack_uint4(packed) -> np.ndarray:
+    """Inverse of pack_uint4."""
+    p = np.ascontiguousarray(np.asarray(packed, dtype=np.uint8))
+    R = p.shape[0]
+    word = p.reshape(R, -1).view("<u4").astype(np.int64)
+    out = np.empty((R, word.shape[1], 8), dtype=np.int64)
+    for i in range(4):
+        out[:, :, 2 * i] = (word >> (4 * i)) & 0xF
+        out[:, :, 2 * i + 1] = (word >> (16 + 4 * i)) & 0xF
+    return out.reshape(R, -1).astype(np.uint8)
+
+
+def unpack_int4(packed, signed: bool = True) -> np.ndarray:
+    """Inverse of pack_int4 (signed); plain nibbles when signed is False."""
     p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
     lo, hi = p & 0xF, p >> 4
     out = np.empty((p.shape[0], p.shape[1] * 2), dtype=np.int64)

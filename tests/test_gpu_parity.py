@@ -193,7 +193,7 @@ def test_weight_quant_asymmetric_bit_exact(group, NK):
         Wb[1, group:2 * group] = 0x3F80  # a constant positive group (1.0)
     q, s, z = vq.quantize_weights_rtn(to_dev_bf16(Wb), 4, False, group, 0)
     ref = o.quantize_weights_rtn(Wb, 4, False, group, 0)
-    np.testing.assert_array_equal(o.unpack_int4(q.cpu().numpy(), signed=False), ref["q"])
+    np.testing.assert_array_equal(o.unpack_uint4(q.cpu().numpy()), ref["q"])
     np.testing.assert_array_equal(o.bf16_to_f64(bf16_bits(s)), ref["s"].astype(np.float64))
     np.testing.assert_array_equal(o.bf16_to_f64(bf16_bits(z)), ref["z"].astype(np.float64))
 
@@ -307,8 +307,9 @@ def test_linear_epilogue_with_oracle_codes(bits):
 
 
 @pytest.mark.parametrize("group", [64, 128, 256])
-@pytest.mark.parametrize("MNK", [(1, 4096, 4096), (4, 256, 1024), (50, 1024, 1024), (50, 1024, 4096),
-                                 (64, 512, 11008), (7, 100, 256)])
+@pytest.mark.parametrize("MNK", [(1, 4096, 4096), (4, 256, 1024), (5, 256, 1024), (50, 1024, 1024),
+                                 (50, 1024, 4096), (50, 8192, 1024), (64, 512, 11008), (7, 100, 256),
+                                 (17, 300, 2048), (129, 264, 1024), (512, 384, 4096)])
 def test_linear_w4a16(group, MNK):
     M, N, K = MNK
     if K % group:

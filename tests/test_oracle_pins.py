@@ -237,9 +237,22 @@ def test_pack_int4_format():
     assert np.array_equal(o.unpack_int4(p, True), codes)
     with pytest.raises(ValueError):
         o.pack_int4(np.array([[-8, 0]], dtype=np.int8))
-    u = np.array([[0, 15, 8, 1]], dtype=np.uint8)
-    assert o.pack_uint4(u)[0].tolist() == [0xF0, 0x18]
-    assert np.array_equal(o.unpack_int4(o.pack_uint4(u), False), u)
+
+
+
+def test_pack_uint4_format():
+    # one 32-bit little-endian word per 8 channels: channel 2i in bits
+    # [4i, 4i+4), channel 2i+1 in bits [16+4i, 16+4i+4)
+    u = np.array([[1, 2, 3, 4, 5, 6, 7, 8, 15, 0, 0, 0, 0, 0, 0, 9]], dtype=np.uint8)
+    p = o.pack_uint4(u)
+    # word 0: evens 1,3,5,7 -> 0x7531; odds 2,4,6,8 -> 0x8642
+    # word 1: evens 15,0,0,0 -> 0x000F; odds 0,0,0,9 -> 0x9000
+    assert p[0].tolist() == [0x31, 0x75, 0x42, 0x86, 0x0F, 0x00, 0x00, 0x90]
+    assert np.array_equal(o.unpack_uint4(p), u)
+    r = random_codes((3, 64), 0, 15, seed=3).astype(np.uint8)
+    assert np.array_equal(o.unpack_uint4(o.pack_uint4(r)), r)
+    with pytest.raises(ValueError):
+        o.pack_uint4(np.array([[16] + [0] * 7]))
 
 
 def test_pack_int8_format():
