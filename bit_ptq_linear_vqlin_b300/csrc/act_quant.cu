@@ -15,6 +15,7 @@
 //   * the per-token absmax is reduced over the token's threads (shuffles, then
 //     shared memory across warps); one CTA holds one or more whole tokens.
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -74,6 +75,8 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
   constexpr int qmax = (1 << (BITS - 1)) - 1;
   __shared__ float red[16];
 
+  pdl_wait();     // X comes from the previous kernel; q and s may still be read by it
+  pdl_trigger();
   const int r = threadIdx.x / tpr;  // token slot inside the CTA
   const int ut = threadIdx.x % tpr;
   const int m = blockIdx.x * rpc + r;
@@ -200,13 +203,19 @@ cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, void* q,
   const int rpc = tpr >= kThreads ? 1 : kThreads / tpr;
   const int threads = rpc * tpr;
   const unsigned grid = vqlin::ceil_div(M, rpc);
-  if (upt == 1)
-    act_quant_kernel<BITS, HB, 1><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
-  else if (upt == 2)
-    act_quant_kernel<BITS, HB, 2><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
-  else
-    act_quant_kernel<BITS, HB, 4><<<grid, threads, 0, st>>>(X, M, K, tpr, rpc, ss, (uint8_t*)q, s);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint8_t* qb = static_cast<uint8_t*>(q);
+  if (upt == 1) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1>, X, M, K, tpr, rpc, ss, qb, s);
+  if (upt == 2) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2>, X, M, K, tpr, rpc, ss, qb, s);
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4>, X, M, K, tpr, rpc, ss, qb, s);
 }
 
 }  // namespace

@@ -32,6 +32,11 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base
                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
                     CUtensorMapSwizzle swizzle);
 
+// Programmatic dependent launch of the library's kernels (on unless the
+// environment sets VQLIN_PDL=0): each kernel may start while the previous one
+// on the stream finishes, and waits for it before touching its outputs.
+bool pdl_enabled();
+
 // Launchers (defined in the kernel files).  They assume validated arguments.
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
                              const float* static_scale, void* q, float* s, cudaStream_t st);

@@ -65,6 +65,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this one depends on (launched before it on the
+// stream with programmatic serialization) have completed and their memory is
+// visible; returns at once when there is no such grid.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid on the stream be scheduled (its CTAs then run up to their
+// own pdl_wait()).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // --------------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -173,6 +184,26 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// TMA store of a 2-D box from shared memory at (x = inner coordinate, y = row);
+// out-of-range parts of the box are not written.  Completed with
+// bulk_commit() + bulk_wait_read().
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(smem_addr(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Barrier among `count` threads (a multiple of 32) of the CTA on barrier `id`.
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // -------------------------------------------------------------------- cluster
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -183,6 +214,21 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of a cluster barrier, for work placed between them.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// 16-byte store into the shared memory of a cluster peer (addresses from
+// mapa) whose completion is counted, in bytes, on the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, int4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
 }
 
 // Address of the same shared-memory location in the CTA of cluster rank `rank`.

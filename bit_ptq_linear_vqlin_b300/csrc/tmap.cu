@@ -1,7 +1,9 @@
-// Host-side encoding of TMA tensor maps through the driver entry point
-// (looked up once through the runtime, so the library links no libcuda).
+// Host-side launch helpers: TMA tensor maps encoded through the driver entry
+// point (looked up once through the runtime, so the library links no
+// libcuda), and the programmatic-dependent-launch switch.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -27,6 +29,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }  // namespace
 
 bool tmap_encoder_available() { return encoder() != nullptr; }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("VQLIN_PDL");
+    return v == nullptr || v[0] != '0';
+  }();
+  return on;
+}
 
 bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -13,6 +13,7 @@
 // reuses them across its 8 rows; partial sums are reduced across lanes at the
 // end.  Every packed weight byte is read from HBM once per token block.
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -27,6 +28,8 @@ __global__ void __launch_bounds__(WARPS * 32)
 w4a16_gemv_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ Wq,
                   const uint16_t* __restrict__ Sg, const uint16_t* __restrict__ Zg,
                   const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K) {
+  pdl_wait();  // X comes from the previous kernel; Y may still be read by it
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n0 = (blockIdx.x * WARPS + warp) * ROWS_PER_WARP;
   const int t0 = blockIdx.y * TOK;
@@ -100,13 +103,20 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* wq, const uint16
                          const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
                          int M, int N, int K, int* /*status*/, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
-  dim3 grid(ceil_div(N, WARPS * ROWS_PER_WARP), ceil_div(M, TOK));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ceil_div(N, WARPS * ROWS_PER_WARP), ceil_div(M, TOK), 1);
+  cfg.blockDim = dim3(WARPS * 32, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (group) {
-    case 64: w4a16_gemv_kernel<64><<<grid, WARPS * 32, 0, st>>>(X, wq, s, z, bias, Y, M, N, K); break;
-    case 128: w4a16_gemv_kernel<128><<<grid, WARPS * 32, 0, st>>>(X, wq, s, z, bias, Y, M, N, K); break;
-    default: w4a16_gemv_kernel<256><<<grid, WARPS * 32, 0, st>>>(X, wq, s, z, bias, Y, M, N, K); break;
+    case 64: return cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<64>, X, wq, s, z, bias, Y, M, N, K);
+    case 128: return cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<128>, X, wq, s, z, bias, Y, M, N, K);
+    default: return cudaLaunchKernelEx(&cfg, w4a16_gemv_kernel<256>, X, wq, s, z, bias, Y, M, N, K);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace vqlin

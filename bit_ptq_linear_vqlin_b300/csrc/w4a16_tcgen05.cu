@@ -126,12 +126,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&opa[i], kUnpackThreads);
+      mbar_init(&opa[i], kUnpackThreads / 32);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], kDrainThreads);
+      mbar_init(&acce[i], kDrainThreads / 32);
     }
     mbar_init(done, 1);
     mbar_init_fence();
@@ -143,6 +143,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  if (tid == 0) pdl_trigger();
 
   float y[BT];
 #pragma unroll
@@ -152,9 +153,21 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < cnt; ++i) {
+      // weight tiles of the first stages before waiting for the previous kernel
+      const int pre = cnt < NS ? cnt : NS;
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* st = base + (size_t)i * kStageBytes;
+        mbar_arrive_expect_tx(&full[i], kStageTx);
+        tma_load_2d(st + kTileN * kOpRow + BT * kOpRow, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        tma_load_2d(base + (size_t)i * kStageBytes + kTileN * kOpRow, &tmX, (kb0 + i) * kKB, m0, &full[i]);
+        ++issued;
+      }
+      for (int i = pre; i < cnt; ++i) {
         const int s = i % NS;
-        if (i >= NS && !mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, a.wait_limit_ns, abort)) {
+        if (!mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
@@ -212,8 +225,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         for (int ii = 0; ii < 8; ++ii) zz[ii] = zero_pair(a, n0 + rbase + 16 * ii, g);
         zg = g;
       }
-      if (!mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
-        if (!*abort) record_timeout(a.status, abort);
+      // warp-uniform exit: the per-warp arrival below needs every lane
+      const bool ok = mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
       uint8_t* st = base + (size_t)s * kStageBytes;
@@ -225,7 +240,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         *reinterpret_cast<uint4*>(st + r * kOpRow + ((c ^ (r & 7)) << 4)) = dequant_word(w, zz[ii]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&opa[s]);
+      __syncwarp();  // one arrival per warp, after every lane's writes and fence
+      if (lane == 0) mbar_arrive(&opa[s]);
     }
   } else {
     // ------------------------------------------------- group drains (warps 6..9)
@@ -251,12 +267,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         for (int j = 0; j < 16; ++j) y[c0 + j] = fmaf(sg, __uint_as_float(v[j]), y[c0 + j]);
       }
       tc_fence_before();
-      mbar_arrive(&acce[jl & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[jl & 1]);
     }
   }
 
   // ---------------------------------------------------------------- epilogue
   __syncwarp();
+  pdl_wait();  // global writes only once the previous kernel has finished
   if (S == 1) {
     if (warp >= 6 && !*abort) {
       const int row = (warp & 3) * 32 + lane, n = n0 + row;
@@ -384,13 +402,15 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes<BT>(NS);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = S;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BT, GROUP>, tmW, tmX, a);
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16 launch (grid %d x %d x %d, %zu B smem): %s", tiles_n, tiles_m, S,
