@@ -317,7 +317,8 @@ class ControlStepStack:
 
         # ---- reusable code / scale / output buffers (one set per group shape)
         def codes(M, K, bits):
-            return torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=dev)
+            # activation codes in the GEMM's operand encoding: a byte (int4) or a 16-bit word (int8) each
+            return torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=dev)
         self.pre_buf = [dict(xq=codes(self.M_pre, g["K"], g["bits"]), sx=torch.empty(self.M_pre, device=dev),
                              y=torch.empty((self.M_pre, g["N"]), dtype=torch.bfloat16, device=dev))
                         for g in self.pre_groups]
@@ -386,12 +387,12 @@ class ControlStepStack:
         kind = key[0]
         if kind.startswith("act_quant"):
             bits, M, K = key[1], key[2], key[3]
-            return 0, 2 * M * K + M * K * bits // 8 + 4 * M
+            return 0, 2 * M * K + M * K * (1 if bits == 4 else 2) + 4 * M
         M, N, K = key[1], key[2], key[3]
         if kind == "linear_w4a4":
-            return 2 * M * N * K, M * K // 2 + N * K // 2 + 4 * M + 4 * N + 2 * M * N
+            return 2 * M * N * K, M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
         if kind == "linear_w8a8":
-            return 2 * M * N * K, M * K + N * K + 4 * M + 4 * N + 2 * M * N
+            return 2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N
         if kind == "linear_w4a16":
             return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // self.group + 2 * M * N
         raise KeyError(key)
@@ -740,25 +741,35 @@ def run_shape(args):
         return torch.randn((r, c), generator=g, device=dev).to(torch.bfloat16)
 
     def rand_codes(r, c, bits):
-        # every byte is a valid sign-magnitude code (a negative zero reads as 0)
+        # weight codes: every byte is a valid sign-magnitude code (a negative zero reads as 0)
         return torch.randint(0, 256, (r, c // 2 if bits == 4 else c), generator=g, device=dev,
                              dtype=torch.int32).to(torch.uint8)
+
+    def rand_act_codes(r, c, bits):
+        # activation codes in the operand encoding: sign bit + magnitude <= qmax
+        qmax = 7 if bits == 4 else 127
+        mag = torch.randint(0, qmax + 1, (r, c), generator=g, device=dev, dtype=torch.int32)
+        sgn = torch.randint(0, 2, (r, c), generator=g, device=dev, dtype=torch.int32)
+        if bits == 4:
+            return (mag | (sgn << 7)).to(torch.uint8)
+        return (mag | (sgn << 15)).to(torch.int16)
 
     group = 128
     if kind.startswith("act_quant"):
         bits = int(kind[-1])
         per = 2 * M * K
-        flops, nbytes = 0, 2 * M * K + M * K * bits // 8 + 4 * M
+        flops, nbytes = 0, 2 * M * K + M * K * (1 if bits == 4 else 2) + 4 * M
         mk = lambda: dict(X=rand_bf16(M, K))  # noqa: E731
-        q = torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=dev)
+        q = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=dev)
         sx = torch.empty(M, device=dev)
         run = lambda d: vq.act_hadamard_quant(d["X"], bits, 128, q_out=q, scale_out=sx)  # noqa: E731
     elif kind in ("linear_w4a4", "linear_w8a8"):
         bits = 4 if kind == "linear_w4a4" else 8
-        kb = K // 2 if bits == 4 else K
+        kb = K // 2 if bits == 4 else K           # packed weight bytes per row
+        xb = K if bits == 4 else 2 * K            # activation operand bytes per token
         per = N * kb
-        flops, nbytes = 2 * M * N * K, M * kb + N * kb + 4 * M + 4 * N + 2 * M * N
-        xq = rand_codes(M, K, bits)
+        flops, nbytes = 2 * M * N * K, M * xb + N * kb + 4 * M + 4 * N + 2 * M * N
+        xq = rand_act_codes(M, K, bits)
         sx = torch.rand(M, generator=g, device=dev)
         mk = lambda: dict(wq=rand_codes(N, K, bits), sw=torch.rand(N, generator=g, device=dev))  # noqa: E731
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)

@@ -8,9 +8,12 @@ the built library, or calling it on CPU tensors, raises.
 
 Tensor conventions (see include/vqlin.h):
   * activations X [M, K] and weights W [N, K] are torch.bfloat16, row-major;
-  * symmetric codes lie in [-qmax, qmax] and are sign-magnitude bytes held
-    in torch.uint8: int4 codes [rows, K/2] (nibble (c < 0) << 3 | |c|, even
-    channel in the low nibble), int8 codes [rows, K] (byte (c < 0) << 7 | |c|);
+  * symmetric codes lie in [-qmax, qmax] and are sign-magnitude: weight
+    codes are torch.uint8, int4 [N, K/2] (nibble (c < 0) << 3 | |c|, even
+    channel in the low nibble) or int8 [N, K] (byte (c < 0) << 7 | |c|);
+    activation codes are in the tensor-core operand encoding, int4 as
+    torch.uint8 [M, K] (byte (c < 0) << 7 | |c|) and int8 as torch.int16
+    [M, K] (bits (c < 0) << 15 | |c|);
   * per-token / per-channel scales are float32; W4A16 group scales and zero
     points are bfloat16 [N, K/group].
 """
@@ -85,7 +88,7 @@ def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_o
     _need(X, "X", torch.bfloat16, 2)
     M, K = X.shape
     if q_out is None:
-        q_out = torch.empty((M, K // 2) if bits == 4 else (M, K), dtype=torch.uint8, device=X.device)
+        q_out = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=X.device)
     if scale_out is None:
         scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
     if static_scale is not None:
@@ -110,17 +113,21 @@ def _linear_int(fn, what, xq, sx, wq, sw, bias, out, K, stream):
 
 
 def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
-    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int4 codes (uint8 [rows, K/2])."""
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias): xq uint8 [M, K], wq uint8 [N, K/2]."""
     _need(xq, "xq", torch.uint8, 2)
     _need(wq, "wq", torch.uint8, 2)
+    if wq.shape[1] * 2 != xq.shape[1]:
+        raise ValueError("wq must be [N, K/2] for xq [M, K]")
     return _linear_int(_lib.vqlin_linear_w4a4, "vqlin_linear_w4a4", xq, sx, wq, sw, bias, out,
-                       xq.shape[1] * 2, stream)
+                       xq.shape[1], stream)
 
 
 def linear_w8a8(xq, sx, wq, sw, bias=None, out=None, stream=None):
-    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias) from int8 codes (uint8 [rows, K])."""
-    _need(xq, "xq", torch.uint8, 2)
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias): xq int16 [M, K], wq uint8 [N, K]."""
+    _need(xq, "xq", torch.int16, 2)
     _need(wq, "wq", torch.uint8, 2)
+    if wq.shape[1] != xq.shape[1]:
+        raise ValueError("wq must be [N, K] for xq [M, K]")
     return _linear_int(_lib.vqlin_linear_w8a8, "vqlin_linear_w8a8", xq, sx, wq, sw, bias, out,
                        xq.shape[1], stream)
 

@@ -35,15 +35,14 @@ __device__ __forceinline__ void butterfly(float& a, float& b) {
   b = d;
 }
 
-// Codes of one 8-channel chunk as sign-magnitude int4 (one word: nibble
-// (c < 0) << 3 | |c|, even channel low) or int8 (two words: byte
-// (c < 0) << 7 | |c|).
+// Codes of one 8-channel chunk in the integer GEMM's operand encoding:
+//   int4: one byte per code, s<<7 | |c| (the e4m3 bits of c * 2^-9) -> w[0..1];
+//   int8: one 16-bit word per code, s<<15 | |c| (the f16 bits of c * 2^-24)
+//         -> w[0..3].
 template <int BITS>
-__device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, float inv_s,
-                                               uint32_t& w0, uint32_t& w1) {
+__device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, float inv_s, uint32_t (&w)[4]) {
   constexpr int qmax = (1 << (BITS - 1)) - 1;
-  w0 = 0;
-  w1 = 0;
+  w[0] = w[1] = w[2] = w[3] = 0;
   if (s == 0.0f) return;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -56,11 +55,9 @@ __device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, flo
     const uint32_t mag = (uint32_t)fabsf(rt);
     const uint32_t neg = rt < 0.0f ? 1u : 0u;
     if (BITS == 4) {
-      w0 |= ((neg << 3) | mag) << (4 * e);
+      w[e >> 2] |= ((neg << 7) | mag) << (8 * (e & 3));
     } else {
-      const uint32_t b = (neg << 7) | mag;
-      if (e < 4) w0 |= b << (8 * e);
-      else w1 |= b << (8 * (e - 4));
+      w[e >> 1] |= ((neg << 15) | mag) << (16 * (e & 1));
     }
   }
 }
@@ -174,13 +171,13 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
     const int g = u / LPG, l = u % LPG;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t w0, w1;
-      quantize_chunk<BITS>(v[i][j], s, inv_s, w0, w1);
+      uint32_t w[4];
+      quantize_chunk<BITS>(v[i][j], s, inv_s, w);
       const size_t ch = (size_t)g * G + (l + LPG * j) * 8;  // first channel of the chunk
       if (BITS == 4) {
-        *reinterpret_cast<uint32_t*>(Q + (size_t)m * (K / 2) + ch / 2) = w0;
+        *reinterpret_cast<uint2*>(Q + (size_t)m * K + ch) = make_uint2(w[0], w[1]);
       } else {
-        *reinterpret_cast<uint2*>(Q + (size_t)m * K + ch) = make_uint2(w0, w1);
+        *reinterpret_cast<uint4*>(Q + ((size_t)m * K + ch) * 2) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }

@@ -99,7 +99,7 @@ using vqlin::fail;
 
 extern "C" {
 
-int vqlin_version(void) { return 200; }
+int vqlin_version(void) { return 300; }
 
 const char* vqlin_status_string(vqlin_status s) {
   switch (s) {
@@ -216,7 +216,7 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
   return linear_int(4, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
 }
 
-vqlin_status vqlin_linear_w8a8(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                const uint16_t* bias, uint16_t* Y, int M, int N, int K, void* stream) {
   return linear_int(8, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
 }

@@ -27,12 +27,18 @@
  *     patterns.  All matrices are row-major: X [M, K], W [N, K] (nn.Linear
  *     layout), Y [M, N].
  *   - Symmetric codes lie in [-qmax, qmax] (qmax = 7 or 127) and are stored
- *     sign-magnitude: an int4 code c is the nibble (c < 0) << 3 | |c|, two
- *     per byte with the even channel k in the low nibble ([rows, K/2]
- *     bytes); an int8 code is the byte (c < 0) << 7 | |c| ([rows, K]).
- *     Asymmetric uint4 codes are plain unsigned nibbles in the same order.
- *     (The pages fix no packing; sign-magnitude codes convert to exact
- *     tensor-core operands with a few bit operations.)
+ *     sign-magnitude.  Weight codes: an int4 code c is the nibble
+ *     (c < 0) << 3 | |c|, two per byte with the even channel k in the low
+ *     nibble ([N, K/2] bytes); an int8 code is the byte (c < 0) << 7 | |c|
+ *     ([N, K]).  Activation codes are stored in the tensor-core operand
+ *     encoding the GEMM consumes unchanged: an int4 code is the byte
+ *     (c < 0) << 7 | |c| ([M, K] bytes, the e4m3 bits of c * 2^-9); an int8
+ *     code is the 16-bit word (c < 0) << 15 | |c| ([M, K] uint16, the f16
+ *     bits of c * 2^-24).  Asymmetric uint4 weight codes (W4A16) hold 8
+ *     channels per little-endian 32-bit word: channel 2i in bits [4i, 4i+4),
+ *     channel 2i+1 in bits [16+4i, 16+4i+4).  (The pages fix no packing;
+ *     these layouts turn into exact tensor-core operands with a few bit
+ *     operations.)
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on it.  Argument checks happen on the host before any
  *     launch; a call that returns an error has launched nothing.
@@ -113,8 +119,9 @@ vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bit
  *   static: s[m] = *static_scale (ONE device float, > 0, finite);
  *   q = clamp(rint(x~ / s), -qmax, qmax), round half to even; s = 0 gives
  *   codes 0.
- * X: bf16 [M, K]; q_out: int4 [M, K/2] bytes (bits 4) or int8 [M, K] (bits 8);
- * scale_out: float [M] (filled with the static scale in static mode).
+ * X: bf16 [M, K]; q_out: [M, K] bytes (bits 4) or [M, K] uint16 (bits 8) in
+ * the activation-code encoding above; scale_out: float [M] (filled with the
+ * static scale in static mode).
  * Requires K % max(b, 32) == 0 and K <= 65536.
  */
 vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
@@ -125,7 +132,8 @@ vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
  * W4A4 projection: Y = bf16( (sum_k xq[m,k] * wq[n,k]) * sx[m] * sw[n] + bias[n] ).
  * The sum is exact in int32; the epilogue is float32 in that order, rounded
  * half to even to bf16.  (FoldQuantVLA abstract: native integer execution.)
- * xq: int4 [M, K/2]; sx: float [M]; wq: int4 [N, K/2]; sw: float [N];
+ * xq: int4 activation codes [M, K] bytes; sx: float [M]; wq: int4 weight
+ * codes [N, K/2]; sw: float [N];
  * bias: bf16 [N] or NULL; Y: bf16 [M, N].  Requires K % 128 == 0 and
  * K <= 65536.  Runs on the tcgen05 tensor cores (int4 codes as exact e4m3
  * operands); K may be split over a thread-block cluster, reduced on chip.
@@ -134,10 +142,11 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);
 
-/* W8A8 projection: as vqlin_linear_w4a4 with int8 codes xq [M, K], wq [N, K]
- * (exact f16 operands; at most 1024 channels per float32 partial sum, which
- * bounds it below 2^24).  Requires K % 64 == 0 and K <= 16384. */
-vqlin_status vqlin_linear_w8a8(const uint8_t* xq, const float* sx, const uint8_t* wq,
+/* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
+ * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands; at
+ * most 1024 channels per float32 partial sum, which bounds it below 2^24).
+ * Requires K % 64 == 0 and K <= 16384. */
+vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq,
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);
 

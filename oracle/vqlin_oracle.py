@@ -43,9 +43,12 @@ The readings taken here (each a plain textbook choice):
   R13 final outputs are rounded once to bf16, round half to even.
 
 Packing (a format of this library; the pages fix none): symmetric codes are
-sign-magnitude -- an int4 code c is the nibble (c < 0) << 3 | |c|, two per
-byte with the even channel in the low nibble; an int8 code is the byte
-(c < 0) << 7 | |c|.  Asymmetric uint4 codes (W4A16) are unsigned nibbles,
+sign-magnitude -- an int4 weight code c is the nibble (c < 0) << 3 | |c|, two
+per byte with the even channel in the low nibble; an int8 weight code is the
+byte (c < 0) << 7 | |c|.  Activation codes use the tensor-core operand
+encoding: one byte (c < 0) << 7 | |c| per int4 code (e4m3 bits of c * 2^-9),
+one 16-bit word (c < 0) << 15 | |c| per int8 code (f16 bits of c * 2^-24).
+Asymmetric uint4 codes (W4A16) are unsigned nibbles,
 eight channels per little-endian 32-bit word: channel 2i in bits [4i, 4i+4),
 channel 2i+1 in bits [16+4i, 16+4i+4).
 """
@@ -312,6 +315,39 @@ def unpack_int8(packed) -> np.ndarray:
     """Inverse of pack_int8."""
     p = np.asarray(packed, dtype=np.uint8).astype(np.int64)
     return np.where(p & 0x80, -(p & 0x7F), p & 0x7F).astype(np.int8)
+
+
+def encode_act_int4(codes) -> np.ndarray:
+    """[M, K] int4 activation codes in [-7, 7] -> [M, K] bytes (c < 0) << 7 | |c|.
+
+    The byte is the e4m3 encoding of c * 2^-9 (a subnormal), which the
+    integer GEMM feeds to the tensor cores unchanged.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    if np.any(np.abs(c) > 7):
+        raise ValueError("int4 codes must lie in [-7, 7]")
+    return (np.where(c < 0, 0x80, 0) | np.abs(c)).astype(np.uint8)
+
+
+def decode_act_int4(enc) -> np.ndarray:
+    e = np.asarray(enc, dtype=np.uint8).astype(np.int64)
+    return np.where(e & 0x80, -(e & 0x7F), e & 0x7F).astype(np.int8)
+
+
+def encode_act_int8(codes) -> np.ndarray:
+    """[M, K] int8 activation codes in [-127, 127] -> [M, K] uint16 (c < 0) << 15 | |c|.
+
+    The word is the f16 encoding of c * 2^-24 (a subnormal).
+    """
+    c = np.asarray(codes).astype(np.int64)
+    if np.any(np.abs(c) > 127):
+        raise ValueError("int8 codes must lie in [-127, 127]")
+    return (np.where(c < 0, 0x8000, 0) | np.abs(c)).astype(np.uint16)
+
+
+def decode_act_int8(enc) -> np.ndarray:
+    e = np.asarray(enc).astype(np.int64) & 0xFFFF
+    return np.where(e & 0x8000, -(e & 0x7FFF), e & 0x7FFF).astype(np.int16)
 
 
 # ----------------------------------------------------------------------------

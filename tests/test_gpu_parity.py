@@ -57,12 +57,27 @@ def rel_fro(a_bits, b_bits):
 
 
 def unpack_codes(q, bits):
+    """Weight codes (packed int4 / int8 bytes) -> int8."""
     q = q.cpu().numpy().view(np.uint8)
     return o.unpack_int4(q, signed=True) if bits == 4 else o.unpack_int8(q)
 
 
+def decode_act(q, bits):
+    """Activation codes (operand encoding) -> integers."""
+    q = q.cpu().numpy()
+    return o.decode_act_int4(q) if bits == 4 else o.decode_act_int8(q.view(np.uint16))
+
+
 def pack_codes(c, bits):
+    """Weight codes -> device bytes."""
     return torch.from_numpy(o.pack_int4(c) if bits == 4 else o.pack_int8(c)).to(DEV)
+
+
+def encode_act(c, bits):
+    """Activation codes -> device operand encoding."""
+    if bits == 4:
+        return torch.from_numpy(o.encode_act_int4(c)).to(DEV)
+    return torch.from_numpy(o.encode_act_int8(c).view(np.int16)).to(DEV)
 
 
 def check_act_codes(q_gpu, s_gpu, Xb, bits, hb, static_scale=None):
@@ -73,7 +88,7 @@ def check_act_codes(q_gpu, s_gpu, Xb, bits, hb, static_scale=None):
         np.testing.assert_array_equal(s_gpu, s_ref)
     else:
         np.testing.assert_allclose(s_gpu, s_ref, rtol=2.0 ** -20, atol=0)
-    q_gpu = unpack_codes(q_gpu, bits)
+    q_gpu = decode_act(q_gpu, bits)
     diff = q_gpu.astype(np.int64) - q_ref.astype(np.int64)
     bad = np.nonzero(diff)
     if hb == 0:
@@ -113,8 +128,7 @@ def test_act_quant_dynamic(bits, case):
     M, K, hb, dist, nout, sc = case
     Xb = activations(M, K, dist=dist, n_outliers=nout, outlier_scale=sc, seed=7, tags=("act", bits))
     X = to_dev_bf16(Xb)
-    shape = (M, K // 2) if bits == 4 else (M, K)
-    qg = Guarded(shape, torch.uint8)
+    qg = Guarded((M, K), torch.uint8 if bits == 4 else torch.int16)
     sg = Guarded((M,), torch.float32)
     vq.act_hadamard_quant(X, bits, hb, q_out=qg.t, scale_out=sg.t)
     qg.check()
@@ -132,7 +146,7 @@ def test_act_quant_static_scale_clamps(bits):
     q, sx = vq.act_hadamard_quant(X, bits, hb, static_scale=st)
     torch.cuda.synchronize()
     check_act_codes(q, sx, Xb, bits, hb, static_scale=s)
-    codes = unpack_codes(q, bits)
+    codes = decode_act(q, bits)
     qmax = 7 if bits == 4 else 127
     assert codes.min() == -qmax or codes.max() == qmax
     assert codes.min() >= -qmax
@@ -149,7 +163,7 @@ def test_act_quant_zero_and_one_hot_rows(bits):
     Xb = f32_to_bf16_bits(x)
     q, s = vq.act_hadamard_quant(to_dev_bf16(Xb), bits, hb)
     torch.cuda.synchronize()
-    codes = unpack_codes(q, bits)
+    codes = decode_act(q, bits)
     assert s[0].item() == 0.0 and not codes[0].any()
     qmax = 7 if bits == 4 else 127
     assert np.all(np.abs(codes[1, 0:128]) == qmax) and not codes[1, 128:].any()
@@ -159,7 +173,7 @@ def test_act_quant_zero_and_one_hot_rows(bits):
 def test_act_quant_empty_is_noop():
     X = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
     q, s = vq.act_hadamard_quant(X, 4, 64)
-    assert q.shape == (0, 128)
+    assert q.shape == (0, 256)
 
 
 # ------------------------------------------------------------ weight quantizer
@@ -215,7 +229,7 @@ def test_int_gemm_bit_exact(bits, shape):
     qmax = 7 if bits == 4 else 127
     xq = random_codes((M, K), -qmax, qmax, seed=1, tags=("x", bits))
     wq = random_codes((N, K), -qmax, qmax, seed=2, tags=("w", bits))
-    xd, wd = pack_codes(xq, bits), pack_codes(wq, bits)
+    xd, wd = encode_act(xq, bits), pack_codes(wq, bits)
     acc = Guarded((M, N), torch.int32)
     vq.debug_gemm_s32(bits, xd, wd, K, out=acc.t)
     acc.check()
@@ -230,7 +244,7 @@ def test_int_gemm_extremes(bits):
     wq = np.full((N, K), -qmax, np.int8)
     wq[1::2, ::2] = qmax                       # large partial sums that cancel late
     wq[2, K // 2:] = 1                         # a large sum, then small additions
-    acc = vq.debug_gemm_s32(bits, pack_codes(xq, bits), pack_codes(wq, bits), K)
+    acc = vq.debug_gemm_s32(bits, encode_act(xq, bits), pack_codes(wq, bits), K)
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
 
 
@@ -242,7 +256,7 @@ def test_int_gemm_bounded_wait_reports_timeout(bits):
     qmax = 7 if bits == 4 else 127
     xq = random_codes((M, K), -qmax, qmax, seed=5)
     wq = random_codes((N, K), -qmax, qmax, seed=6)
-    xd, wd = pack_codes(xq, bits), pack_codes(wq, bits)
+    xd, wd = encode_act(xq, bits), pack_codes(wq, bits)
     vq.get_last_device_error()
     vq.debug_gemm_withheld_loads(bits, xd, wd, K, limit_ns=10_000_000)
     with pytest.raises(vq.VqlinError, match="TIMEOUT"):
@@ -298,7 +312,7 @@ def test_linear_epilogue_with_oracle_codes(bits):
     bias = weights(1, N, std=0.5, seed=33)[0]
     ref = o.linear_quantized(Xb, Wb, bits, 128, bias_bits=bias)
     fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
-    y = fn(pack_codes(ref["xq"], bits), torch.from_numpy(ref["sx"]).to(DEV),
+    y = fn(encode_act(ref["xq"], bits), torch.from_numpy(ref["sx"]).to(DEV),
            pack_codes(ref["wq"], bits), torch.from_numpy(ref["sw"]).to(DEV),
            to_dev_bf16(bias))
     yb = bf16_bits(y).astype(np.int64)

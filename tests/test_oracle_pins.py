@@ -240,6 +240,25 @@ def test_pack_int4_format():
 
 
 
+def test_activation_code_encodings_are_exact_float_operands():
+    # int4 activation code c -> byte (c < 0) << 7 | |c|, the e4m3 bits of
+    # c * 2^-9 (exponent field 0: value (-1)^s * m * 2^-9); int8 -> 16-bit
+    # (c < 0) << 15 | |c|, the f16 bits of c * 2^-24 (value (-1)^s * m * 2^-24)
+    c4 = np.arange(-7, 8).reshape(1, -1)
+    e4 = o.encode_act_int4(c4)
+    assert e4[0].tolist()[:3] == [0x87, 0x86, 0x85] and e4[0, 7] == 0 and e4[0, 14] == 0x07
+    sign = np.where(e4 & 0x80, -1.0, 1.0)
+    assert np.array_equal(sign * (e4 & 0x07) * 2.0 ** -9, c4 * 2.0 ** -9)
+    assert np.array_equal(o.decode_act_int4(e4), c4)
+    c8 = np.array([[-127, -64, -1, 0, 1, 100, 127]])
+    e8 = o.encode_act_int8(c8)
+    assert e8[0].tolist() == [0x807F, 0x8040, 0x8001, 0, 1, 100, 127]
+    assert np.array_equal(e8.view(np.float16).astype(np.float64), c8 * 2.0 ** -24)
+    assert np.array_equal(o.decode_act_int8(e8), c8)
+    with pytest.raises(ValueError):
+        o.encode_act_int4(np.array([[8]]))
+
+
 def test_pack_uint4_format():
     # one 32-bit little-endian word per 8 channels: channel 2i in bits
     # [4i, 4i+4), channel 2i+1 in bits [16+4i, 16+4i+4)
