@@ -37,6 +37,11 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base
 // on the stream finishes, and waits for it before touching its outputs.
 bool pdl_enabled();
 
+// How many clusters of `cluster` CTAs of `kernel` (threads, dynamic shared
+// memory) can be resident on the current device at once (cached; 0 if the
+// query fails).
+int max_active_clusters(const void* kernel, int threads, size_t dyn_smem, int cluster);
+
 // Launchers (defined in the kernel files).  They assume validated arguments.
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
                              const float* static_scale, void* q, float* s, cudaStream_t st);

@@ -439,35 +439,44 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + bt - 1) / bt;
   const int nkb = K / kb_codes;
   const int s_min = BITS == 8 ? (K + 1023) / 1024 : 1;
-  int S = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
-  S = S < s_min ? s_min : S;
-  S = S > kMaxSplit ? kMaxSplit : S;
-  S = S > nkb ? nkb : S;
-  if (S < s_min)  // host checks keep K <= 16384 for int8
+  int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
+  s_want = s_want < s_min ? s_min : s_want;
+  s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
+  s_want = s_want > nkb ? nkb : s_want;
+  if (s_want < s_min)  // host checks keep K <= 16384 for int8
     return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: K=%d needs %d-way split", K, s_min);
-  const int per_cta = (nkb + S - 1) / S;
-  const int rows_per = S > 1 ? ((kTileN + S - 1) / S + 3) & ~3 : kTileN;
-  // stages: up to 6 within the shared-memory limit, no more than the k-blocks
-  // a CTA runs, and enough that the int32 partial tile of the split-K
-  // epilogue ([bt][128] int32) fits over them
-  const int ns_min = (int)(((size_t)bt * kTileN * 4 + stage_bytes(bt) - 1) / stage_bytes(bt));
-  int NS = per_cta > 6 ? 6 : per_cta;
-  if (NS < ns_min) NS = ns_min;
-  if (NS < 2) NS = 2;
-  while (NS > ns_min && NS > 2 && smem_bytes(bt, NS) > (size_t)kMaxSmem) --NS;
-  // tensor memory: accumulator [0, bt) then one 32-column A slot per stage
-  const uint32_t a_col = (uint32_t)((bt + 31) / 32 * 32);
-  uint32_t cols = 32;
-  while (cols < a_col + (uint32_t)(NS * kACols)) cols <<= 1;
-  if (cols > 512 || smem_bytes(bt, NS) > (size_t)kMaxSmem)
-    return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: no tile plan for M=%d N=%d K=%d", M, N, K);
-  // never more CTAs on an SM than its 512 tensor-memory columns hold: a CTA
-  // blocked in tcgen05.alloc while its cluster peers wait for it could
-  // otherwise wait on CTAs of another cluster in the same state
-  size_t dyn = smem_bytes(bt, NS);
-  const size_t fit = 512 / cols;
-  const size_t dyn_floor = kSmemPerSm / (fit + 1) + 1;
-  if (dyn < dyn_floor) dyn = dyn_floor;
+  // the largest split whose clusters are all resident at once (one wave);
+  // the smallest allowed one if none is
+  int S = 0, NS = 0, rows_per = 0;
+  uint32_t a_col = 0, cols = 0;
+  size_t dyn = 0;
+  for (int s_try = s_want; s_try >= s_min; --s_try) {
+    const int per_cta = (nkb + s_try - 1) / s_try;
+    // stages: up to 6 within the shared-memory limit, no more than the
+    // k-blocks a CTA runs, and enough that the int32 partial tile of the
+    // split-K epilogue ([bt][128] int32) fits over them
+    const int ns_min = (int)(((size_t)bt * kTileN * 4 + stage_bytes(bt) - 1) / stage_bytes(bt));
+    int ns = per_cta > 6 ? 6 : per_cta;
+    if (ns < ns_min) ns = ns_min;
+    if (ns < 2) ns = 2;
+    while (ns > ns_min && ns > 2 && smem_bytes(bt, ns) > (size_t)kMaxSmem) --ns;
+    // tensor memory: accumulator [0, bt) then one 32-column A slot per stage
+    const uint32_t ac = (uint32_t)((bt + 31) / 32 * 32);
+    uint32_t c = 32;
+    while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
+    if (c > 512 || smem_bytes(bt, ns) > (size_t)kMaxSmem) continue;
+    // never more CTAs on an SM than its 512 tensor-memory columns hold: a CTA
+    // blocked in tcgen05.alloc while its cluster peers wait for it could
+    // otherwise wait on CTAs of another cluster in the same state
+    size_t d = smem_bytes(bt, ns);
+    const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
+    if (d < dyn_floor) d = dyn_floor;
+    S = s_try; NS = ns; a_col = ac; cols = c; dyn = d;
+    rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+    const int active = vqlin::max_active_clusters((const void*)qgemm_kernel<BITS>, kThreads, d, s_try);
+    if (tiles_n * tiles_m <= active) break;
+  }
+  if (S == 0) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: no tile plan for M=%d N=%d K=%d", M, N, K);
   const bool tma_store = S == 1 && acc == nullptr && (N % 8) == 0;
 
   CUtensorMap tmW, tmX, tmY;

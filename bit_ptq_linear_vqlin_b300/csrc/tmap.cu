@@ -4,7 +4,9 @@
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 
@@ -29,6 +31,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }  // namespace
 
 bool tmap_encoder_available() { return encoder() != nullptr; }
+
+int max_active_clusters(const void* kernel, int threads, size_t dyn_smem, int cluster) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, size_t, int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(kernel, threads, dyn_smem, cluster, dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, cluster);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = dyn_smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = cluster;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
+}
 
 bool pdl_enabled() {
   static const bool on = [] {

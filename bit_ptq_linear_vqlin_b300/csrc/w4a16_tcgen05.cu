@@ -18,15 +18,16 @@
 // subtraction of 128 + z leaves q - z exactly.
 //
 // Work decomposition (weights on the MMA's M side):
-//   * one CTA: 128 output channels x BT tokens (BT in {16, 32, 64}) over
-//     a range of whole groups of K; the S CTAs that split K form a cluster;
-//   * warp 0: TMA producer; each stage holds the packed weight tile (32 bytes
-//     of each row per 64-channel k-block) and the activation tile, which TMA
-//     writes directly in the 128-byte swizzled MMA layout;
-//   * warps 2..5: unpack the weight tile into bf16 (q - z) operand rows;
-//   * warp 1: tensor memory and the MMAs (kind::f16, bf16 x bf16 -> f32), one
-//     accumulator per group, double-buffered;
-//   * warps 6..9: drain each group's accumulator, y += s[n,g] * partial, in
+//   * one CTA: 128 output channels x BT tokens (BT in {16, 32, 64}) over a
+//     range of whole groups of K; the S CTAs that split K form a cluster;
+//   * warp 0: TMA producer; a stage holds the activation tile (bf16, written
+//     by TMA directly in the 128-byte-swizzled MMA layout) and the packed
+//     weight tile (32 bytes of each row per 64-channel k-block);
+//   * warps 2..9: expand the packed weights into bf16 (q - z) directly in
+//     tensor memory (thread = weight row, tcgen05.st), the MMA's A operand;
+//   * warp 1: tensor memory and the MMAs (kind::f16, bf16 x bf16 -> f32, A
+//     from tensor memory), one accumulator per group, double-buffered;
+//   * warps 10..13: drain each group's accumulator, y += s[n,g] * partial, in
 //     registers; then the bias epilogue, with split K summed over the
 //     cluster's shared memory in a fixed order (deterministic).
 // Every wait is bounded in time (VQLIN_ERR_TIMEOUT in the status word).
@@ -42,9 +43,10 @@ using namespace vqlin_dev;
 constexpr int kTileN = 128;
 constexpr int kKB = 64;           // channels per k-block (one 128-byte bf16 row)
 constexpr int kRawRow = 32;       // packed weight bytes of one row per k-block
-constexpr int kOpRow = 128;
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kUnpackThreads = 128;
+constexpr int kBRow = 128;        // activation bytes of one row per k-block
+constexpr int kACols = 32;        // tensor-memory columns of one A stage
+constexpr int kThreads = 448;     // 14 warps
+constexpr int kExpandWarps = 8;
 constexpr int kDrainThreads = 128;
 constexpr int kMaxSplit = 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -58,6 +60,8 @@ struct W4a16Args {
   int M, N, K, G;          // G = K / group
   int stages;
   uint32_t tmem_cols;
+  uint32_t a_col;          // first tensor-memory column of the A stages
+  int rows_per;            // split K: output channels each cluster rank owns
   uint64_t wait_limit_ns;
 };
 
@@ -72,14 +76,12 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   return d;
 }
 
-// 8 packed codes (one word) -> 8 bf16 values q - z (16 bytes), channel order.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zz) {
-  uint4 o;
-  o.x = bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zz);
-  o.y = bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zz);
-  o.z = bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zz);
-  o.w = bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zz);
-  return o;
+// 8 packed codes (one word) -> 8 bf16 values q - z (4 words), channel order.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zz, uint32_t* o) {
+  o[0] = bf16x2_sub((w & 0x000F000Fu) | 0x43004300u, zz);
+  o[1] = bf16x2_sub(((w >> 4) & 0x000F000Fu) | 0x43004300u, zz);
+  o[2] = bf16x2_sub(((w >> 8) & 0x000F000Fu) | 0x43004300u, zz);
+  o[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zz);
 }
 
 // bf16x2 bit pattern of (128 + z, 128 + z) for the zero point of row n, group g.
@@ -95,17 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const W4a16Args a) {
   constexpr int KB_PER_G = GROUP / kKB;
-  constexpr uint32_t kStageTx = kTileN * kRawRow + BT * kOpRow;
+  constexpr uint32_t kBBytes = BT * kBRow;                       // a multiple of 2048
+  constexpr uint32_t kStageBytes = kBBytes + kTileN * kRawRow;   // [B operand | packed A]
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  constexpr uint32_t kStageBytes = kTileN * kOpRow + BT * kOpRow + kTileN * kRawRow;  // opA | opB | rawA
   const int NS = a.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * kStageBytes);
-  uint64_t* full = bars;              // TMA -> unpack
-  uint64_t* opa = bars + NS;          // unpack -> MMA
+  uint64_t* full = bars;              // TMA -> expanders
+  uint64_t* aready = bars + NS;       // expanders -> MMA
   uint64_t* empty = bars + 2 * NS;    // MMA -> TMA
   uint64_t* accf = bars + 3 * NS;     // [2] MMA -> drain
   uint64_t* acce = accf + 2;          // [2] drain -> MMA
@@ -126,7 +128,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&opa[i], kUnpackThreads / 32);
+      mbar_init(&aready[i], kExpandWarps);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -156,13 +158,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       // weight tiles of the first stages before waiting for the previous kernel
       const int pre = cnt < NS ? cnt : NS;
       for (int i = 0; i < pre; ++i) {
-        uint8_t* st = base + (size_t)i * kStageBytes;
-        mbar_arrive_expect_tx(&full[i], kStageTx);
-        tma_load_2d(st + kTileN * kOpRow + BT * kOpRow, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
+        mbar_arrive_expect_tx(&full[i], kStageBytes);
+        tma_load_2d(base + (size_t)i * kStageBytes + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
-        tma_load_2d(base + (size_t)i * kStageBytes + kTileN * kOpRow, &tmX, (kb0 + i) * kKB, m0, &full[i]);
+        tma_load_2d(base + (size_t)i * kStageBytes, &tmX, (kb0 + i) * kKB, m0, &full[i]);
         ++issued;
       }
       for (int i = pre; i < cnt; ++i) {
@@ -172,9 +173,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           break;
         }
         uint8_t* st = base + (size_t)s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageTx);
-        tma_load_2d(st + kTileN * kOpRow + BT * kOpRow, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
-        tma_load_2d(st + kTileN * kOpRow, &tmX, (kb0 + i) * kKB, m0, &full[s]);
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tma_load_2d(st + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
+        tma_load_2d(st, &tmX, (kb0 + i) * kKB, m0, &full[s]);
         ++issued;
       }
       for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
@@ -185,8 +186,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
-      bool ok = true;
-      for (int i = 0; i < cnt && ok; ++i) {
+      for (int i = 0; i < cnt; ++i) {
         const int s = i % NS;
         const int jl = i / KB_PER_G, kin = i % KB_PER_G;  // local group, k-block inside it
         const uint32_t acc = tmem + (uint32_t)((jl & 1) * BT);
@@ -195,56 +195,57 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
-        if (!mbar_wait_bounded(&opa[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
+        if (!mbar_wait_bounded(&aready[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
         tc_fence_after();
-        const uint8_t* st = base + (size_t)s * kStageBytes;
-        const uint64_t da = sdesc_sw128(st), db = sdesc_sw128(st + kTileN * kOpRow);
+        const uint64_t db = sdesc_sw128(base + (size_t)s * kStageBytes);
+        const uint32_t ta = tmem + a.a_col + (uint32_t)(s * kACols);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mma_f16(acc, da + 2 * j, db + 2 * j, id, (kin | j) != 0);
+        for (int j = 0; j < 4; ++j) mma_f16_ta(acc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
         tc_commit(&empty[s]);
         if (kin == KB_PER_G - 1) tc_commit(&accf[jl & 1]);
       }
-      (void)ok;
       tc_commit(done);  // tensor memory is freed only after this completes
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ unpackers
-    // thread t: word c = t % 8 of rows t/8 + 16 i, i = 0..7 (fixed rows, so the
-    // zero points of a group are loaded once per group)
-    const int t = tid - 64, c = t & 7, rbase = t >> 3;
-    uint32_t zz[8];
-    int zg = -1;
+  } else if (warp < 10) {
+    // ------------------------------------------------- weight expanders (2..9)
+    // thread = weight row; the two warps of a lane quadrant take the two
+    // 16-byte halves of the row's 32 packed bytes (64 channels)
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = q * 32 + lane, n = n0 + row;
+    const int chunk = h ^ ((row >> 2) & 1);  // 32-byte swizzle of the packed tile
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col + (uint32_t)(16 * h);
+    uint32_t zz = ng > 0 ? zero_pair(a, n, g0) : 0u;
+    uint32_t zz_next = ng > 1 ? zero_pair(a, n, g0 + 1) : 0u;
     for (int i = 0; i < cnt; ++i) {
       const int s = i % NS;
-      const int g = g0 + i / KB_PER_G;
-      if (g != zg) {
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii) zz[ii] = zero_pair(a, n0 + rbase + 16 * ii, g);
-        zg = g;
-      }
-      // warp-uniform exit: the per-warp arrival below needs every lane
       const bool ok = mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
-      uint8_t* st = base + (size_t)s * kStageBytes;
-      const uint8_t* raw = st + kTileN * kOpRow + BT * kOpRow;
-#pragma unroll
-      for (int ii = 0; ii < 8; ++ii) {
-        const int r = rbase + 16 * ii;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + r * kRawRow + c * 4);
-        *reinterpret_cast<uint4*>(st + r * kOpRow + ((c ^ (r & 7)) << 4)) = dequant_word(w, zz[ii]);
+      const uint4 c = *reinterpret_cast<const uint4*>(base + (size_t)s * kStageBytes + kBBytes + row * kRawRow +
+                                                      (chunk << 4));
+      uint32_t v[16];
+      dequant_word(c.x, zz, v);
+      dequant_word(c.y, zz, v + 4);
+      dequant_word(c.z, zz, v + 8);
+      dequant_word(c.w, zz, v + 12);
+      tmem_st_x16(trow + (uint32_t)(s * kACols), v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aready[s]);
+      if (i % KB_PER_G == KB_PER_G - 1) {  // next group: rotate the zero points
+        const int jn = i / KB_PER_G + 2;
+        zz = zz_next;
+        zz_next = jn < ng ? zero_pair(a, n, g0 + jn) : 0u;
       }
-      fence_proxy_async_smem();
-      __syncwarp();  // one arrival per warp, after every lane's writes and fence
-      if (lane == 0) mbar_arrive(&opa[s]);
     }
   } else {
-    // ------------------------------------------------- group drains (warps 6..9)
+    // ------------------------------------------------ group drains (10..13)
     const int q = warp & 3, row = q * 32 + lane, n = n0 + row;
     float sg_next = 0.0f;
     if (ng > 0 && n < a.N) sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0) << 16);
@@ -276,7 +277,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   __syncwarp();
   pdl_wait();  // global writes only once the previous kernel has finished
   if (S == 1) {
-    if (warp >= 6 && !*abort) {
+    if (warp >= 10 && !*abort) {
       const int row = (warp & 3) * 32 + lane, n = n0 + row;
       if (n < a.N) {
         const float b = a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n) << 16) : 0.0f;
@@ -288,10 +289,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     tc_fence_before();
     __syncthreads();
   } else {
-    // float partial tile part[token][channel] over the idle stage ring
+    // float partial tile part[token][channel] over the idle stages
     float* part = reinterpret_cast<float*>(base);
-    __syncthreads();  // every role is past the ring before it is overwritten
-    if (warp >= 6 && !*abort) {
+    __syncthreads();  // every role is past the stages before they are overwritten
+    if (warp >= 10 && !*abort) {
       const int row = (warp & 3) * 32 + lane;
 #pragma unroll
       for (int c = 0; c < BT; ++c) part[c * kTileN + row] = y[c];
@@ -299,7 +300,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     tc_fence_before();
     cluster_sync_all();
     if (!*abort) {
-      const int rows_per = ((kTileN + S - 1) / S + 3) & ~3;
+      const int rows_per = a.rows_per;
       const int r0 = (int)rank * rows_per;
       const int nq = (min(kTileN, r0 + rows_per) - r0) / 4;
       const uint32_t part_s = smem_addr(part);
@@ -347,10 +348,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 // ------------------------------------------------------------------ host side
 
 constexpr int kMaxSmem = 232448 - 4096;
+constexpr size_t kSmemPerSm = 233472;
 
 template <int BT>
 constexpr size_t stage_bytes() {
-  return (size_t)kTileN * kOpRow + (size_t)BT * kOpRow + (size_t)kTileN * kRawRow;
+  return (size_t)BT * kBRow + (size_t)kTileN * kRawRow;
 }
 
 template <int BT>
@@ -372,35 +374,55 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + BT - 1) / BT;
   const int G = K / GROUP;
-  int S = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
-  S = S > kMaxSplit ? kMaxSplit : S;
-  S = S > G ? G : S;
-  const int per_cta = (G + S - 1) / S * (GROUP / kKB);
-  int NS = 6;
-  while (NS > 2 && smem_bytes<BT>(NS) > (size_t)kMaxSmem) --NS;
-  if (NS > per_cta) NS = per_cta < 2 ? 2 : per_cta;
-  // the float partial tile of the split-K epilogue overlays the stage ring
-  static_assert(2 * stage_bytes<BT>() >= (size_t)BT * kTileN * 4, "partial tile must fit two stages");
-  uint32_t cols = 32;
-  while ((int)cols < 2 * BT) cols <<= 1;
+  int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
+  s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
+  s_want = s_want > G ? G : s_want;
+  // the largest split whose clusters are all resident at once (one wave)
+  int S = 0, NS = 0, rows_per = 0;
+  uint32_t a_col = 0, cols = 0;
+  size_t dyn = 0;
+  for (int s_try = s_want; s_try >= 1; --s_try) {
+    const int per_cta = (G + s_try - 1) / s_try * (GROUP / kKB);
+    // stages: up to 4, no more than the k-blocks a CTA runs, and enough that
+    // the float partial tile of the split-K epilogue ([BT][128]) fits over them
+    const int ns_min = (int)(((size_t)BT * kTileN * 4 + stage_bytes<BT>() - 1) / stage_bytes<BT>());
+    int ns = per_cta > 4 ? 4 : per_cta;
+    if (ns < ns_min) ns = ns_min;
+    if (ns < 2) ns = 2;
+    // tensor memory: two group accumulators [0, 2 BT), then one A slot per stage
+    const uint32_t ac = (uint32_t)((2 * BT + 31) / 32 * 32);
+    uint32_t c = 32;
+    while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
+    if (c > 512 || smem_bytes<BT>(ns) > (size_t)kMaxSmem) continue;
+    // never more CTAs on an SM than its tensor memory holds (see the integer GEMM)
+    size_t d = smem_bytes<BT>(ns);
+    const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
+    if (d < dyn_floor) d = dyn_floor;
+    S = s_try; NS = ns; a_col = ac; cols = c; dyn = d;
+    rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+    const int active = vqlin::max_active_clusters((const void*)w4a16_tc_kernel<BT, GROUP>, kThreads, d, s_try);
+    if (tiles_n * tiles_m <= active) break;
+  }
+  if (S == 0) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "w4a16: no tile plan for M=%d N=%d K=%d", M, N, K);
 
   CUtensorMap tmW, tmX;
   if (!vqlin::tmap_encoder_available())
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: cuTensorMapEncodeTiled is unavailable");
   if (!vqlin::encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
-                             kRawRow, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                             kRawRow, kTileN, CU_TENSOR_MAP_SWIZZLE_32B) ||
       !vqlin::encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
                              kKB, BT, CU_TENSOR_MAP_SWIZZLE_128B))
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
 
   W4a16Args a;
   a.scales = s; a.zeros = z; a.bias = bias; a.Y = Y; a.status = status;
-  a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.wait_limit_ns = kWaitLimitNs;
+  a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
+  a.rows_per = rows_per; a.wait_limit_ns = kWaitLimitNs;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, S);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes<BT>(NS);
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
