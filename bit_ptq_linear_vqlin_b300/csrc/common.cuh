@@ -72,7 +72,7 @@ constexpr int kW4a16GemvMaxM = 4;
 constexpr int kActQuantMaxK = 65536;
 constexpr int kWeightQuantMaxK = 49152;
 constexpr int kGemmW4MaxK = 65536;   // |acc| <= 49 K stays below 2^24
-constexpr int kGemmW8MaxK = 16384;   // 1024 channels per CTA x 16 CTAs per cluster
+constexpr int kGemmW8MaxK = 65536;   // |acc| <= 127^2 K stays below 2^31
 
 }  // namespace vqlin
 

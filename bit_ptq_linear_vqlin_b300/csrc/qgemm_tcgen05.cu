@@ -14,8 +14,10 @@
 //     exactly (|acc| <= 49 K < 2^24 for K < 342k);
 //   * int8 code c (|c| <= 127) is the f16 subnormal s<<15 | |c|, value
 //     c * 2^-24; the MMA is kind::f16 and the accumulator holds acc * 2^-48
-//     exactly while |acc| <= 127^2 * 1024 < 2^24, so every CTA sums at most
-//     1024 channels and longer K is split across the cluster.
+//     exactly while |acc| <= 127^2 * 1024 < 2^24, so the MMAs accumulate
+//     1024 channels at a time into one of two float32 buffers in tensor
+//     memory, and the expander warps add each finished chunk, converted to
+//     int32, into an int32 running sum there (exact for any K).
 // Activation codes arrive already in that operand encoding (one byte per int4
 // code, one 16-bit word per int8 code, written so by the activation kernel),
 // so TMA copies them straight into the 128-byte-swizzled MMA layout.  Weight
@@ -72,6 +74,9 @@ struct QgemmArgs {
   int stages;
   uint32_t tmem_cols;
   uint32_t a_col;        // first tensor-memory column of the A stages
+  int chunk_kb;          // > 0: exact int32 chunking every chunk_kb k-blocks (int8)
+  uint32_t d1_col;       // chunking: second float32 accumulator
+  uint32_t r_col;        // chunking: int32 running sum
   uint64_t wait_limit_ns;
   int withhold_loads;    // test hook: the producer issues nothing (waits run out)
   int tma_store;         // unsplit K: stage the bf16 tile and store it with TMA
@@ -129,6 +134,8 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   uint64_t* empty = bars + 2 * NS;     // MMA -> TMA (stage consumed)
   uint64_t* acc_full = bars + 3 * NS;
   uint64_t* scl_ready = acc_full + 1;
+  uint64_t* accf = acc_full + 2;       // [2] chunking: MMA -> drain (chunk accumulated)
+  uint64_t* acce = acc_full + 4;       // [2] chunking: drain -> MMA (accumulator free)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z;
@@ -148,6 +155,10 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     }
     mbar_init(acc_full, 1);
     mbar_init(scl_ready, 31);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], kExpandWarps);
+    }
     mbar_init_fence();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -215,8 +226,19 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_f32acc(0u, kTileN, bt);  // e4m3 x e4m3 or f16 x f16 -> f32
+      const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
       for (int i = 0; i < cnt; ++i) {
         const int s = i % NS;
+        // chunking: chunk c accumulates into float32 buffer c & 1, which the
+        // expanders drain into the int32 running sum before chunk c + 2 reuses it
+        const int ckd = ck > 0 ? ck : 1;
+        const int c = ck ? i / ckd : 0, kin = ck ? i % ckd : i;
+        const uint32_t dacc = tmem + ((c & 1) ? a.d1_col : 0u);
+        if (ck && kin == 0 && c >= 2 &&
+            !mbar_wait_bounded(&acce[c & 1], ((c >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
+          if (!*abort) record_timeout(a.status, abort);
+          break;
+        }
         if (!mbar_wait_bounded(&aready[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
@@ -227,10 +249,11 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // per MMA: 8 tensor-memory columns of A, 32 bytes along the swizzled B row
-          if (BITS == 4) mma_f8f6f4_ta(tmem, ta + 8 * j, db + 2 * j, id, (i | j) != 0);
-          else mma_f16_ta(tmem, ta + 8 * j, db + 2 * j, id, (i | j) != 0);
+          if (BITS == 4) mma_f8f6f4_ta(dacc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
+          else mma_f16_ta(dacc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
         }
         tc_commit(&empty[s]);
+        if (ck && (kin == ck - 1 || i == cnt - 1)) tc_commit(&accf[c & 1]);
       }
       tc_commit(acc_full);
     }
@@ -241,7 +264,37 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const int sw = (row >> 1) & 3;  // 64-byte swizzle of the packed tile
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col + (uint32_t)(16 * h);
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t trow = lanes + a.a_col + (uint32_t)(16 * h);
+    const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
+    const float unit = 281474976710656.0f;  // 2^48: f16-operand accumulator -> integer
+    // chunking: adds float32 chunk c (exact integers x 2^-48, each below 2^24)
+    // into the int32 running sum; this warp takes columns 16h, 16h + 32, ...
+    auto drain = [&](int c) -> bool {
+      const bool okc = mbar_wait_bounded(&accf[c & 1], (c >> 1) & 1, a.wait_limit_ns, abort);
+      if (!__all_sync(0xffffffffu, okc)) {
+        if (!okc && !*abort) record_timeout(a.status, abort);
+        return false;
+      }
+      tc_fence_after();
+      const uint32_t src = lanes + ((c & 1) ? a.d1_col : 0u);
+      for (int c0 = 16 * h; c0 < bt; c0 += 32) {
+        uint32_t v[16], r[16];
+        tmem_ld_x16(src + (uint32_t)c0, v);
+        if (c > 0) tmem_ld_x16(lanes + a.r_col + (uint32_t)c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          r[j] = (uint32_t)((c > 0 ? (int32_t)r[j] : 0) + __float2int_rn(__uint_as_float(v[j]) * unit));
+        tmem_st_x16(lanes + a.r_col + (uint32_t)c0, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[c & 1]);
+      return true;
+    };
+    bool ok_all = true;
     for (int i = 0; i < cnt; ++i) {
       const int s = i % NS;
       const bool ok = mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort);
@@ -262,7 +315,16 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aready[s]);
+      if (ck > 0) {
+        const int ckd = ck > 0 ? ck : 1;  // (a divisor the compiler sees as non-zero)
+        if (i >= ckd && i % ckd == 0 && !drain(i / ckd - 1)) {
+          ok_all = false;
+          break;
+        }
+        if (i == cnt - 1 && !drain(i / ckd)) ok_all = false;
+      }
     }
+    (void)ok_all;
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -283,6 +345,22 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   const int q = warp & 3;
   const int h = (warp - 2) >> 2;
   const int row = q * 32 + lane;   // output channel inside the tile
+  // 16 int32 accumulators of this thread's row, columns c0 .. c0 + 15
+  auto load_acc = [&](int c0, int32_t (&out)[16]) {
+    uint32_t v[16];
+    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+    if (BITS == 8 && a.chunk_kb) {
+      tmem_ld_x16(lanes + a.r_col + (uint32_t)c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[j] = (int32_t)v[j];
+    } else {
+      tmem_ld_x16(lanes + (uint32_t)c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[j] = __float2int_rn(__uint_as_float(v[j]) * unit);
+    }
+  };
 
   if (S == 1 && a.tma_store) {
     // bf16 tile [bt tokens][128 channels] staged over the idle stages, then one
@@ -292,12 +370,11 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       if (go) {
         const float sw_n = s_sw[row], b_n = s_bias[row];
         for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-          uint32_t v[16];
-          tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-          tmem_ld_wait();
+          int32_t v[16];
+          load_acc(c0, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float acc = (float)__float2int_rn(__uint_as_float(v[j]) * unit);
+            const float acc = (float)v[j];
             ystage[(c0 + j) * kTileN + row] =
                 f32_to_bf16_rn(__fadd_rn(__fmul_rn(__fmul_rn(acc, s_sx[c0 + j]), sw_n), b_n));
           }
@@ -320,15 +397,14 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       const int n = n0 + row;
       const float sw_n = s_sw[row], b_n = s_bias[row];
       for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-        tmem_ld_wait();
+        int32_t v[16];
+        load_acc(c0, v);
         if (n < a.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
             if (m < a.M) {
-              const int32_t acc = __float2int_rn(__uint_as_float(v[j]) * unit);
+              const int32_t acc = v[j];
               if (raw_out) {
                 a.acc[(size_t)m * a.N + n] = acc;
               } else {
@@ -350,11 +426,10 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     int32_t* part = reinterpret_cast<int32_t*>(base);
     if (warp >= 2 && go) {
       for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-        tmem_ld_wait();
+        int32_t v[16];
+        load_acc(c0, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) part[(c0 + j) * kTileN + row] = __float2int_rn(__uint_as_float(v[j]) * unit);
+        for (int j = 0; j < 16; ++j) part[(c0 + j) * kTileN + row] = v[j];
       }
     }
     tc_fence_before();
@@ -416,7 +491,7 @@ constexpr size_t kSmemPerSm = 233472;  // shared memory of one SM
 
 size_t stage_bytes(int bt) { return (size_t)bt * kBRow + (size_t)kTileN * kRawRow; }
 
-size_t smem_bytes(int bt, int stages) { return 1024 + stages * stage_bytes(bt) + (3 * stages + 2) * 8; }
+size_t smem_bytes(int bt, int stages) { return 1024 + stages * stage_bytes(bt) + (3 * stages + 6) * 8; }
 
 template <int BITS>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
@@ -434,49 +509,90 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
 
   const int kb_codes = BITS == 4 ? 128 : 64;
   const int w_row_bytes = BITS == 4 ? K / 2 : K;
-  const int nt = (M + 255) / 256;
-  const int bt = ((M + nt - 1) / nt + 15) / 16 * 16;
-  const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + bt - 1) / bt;
   const int nkb = K / kb_codes;
-  const int s_min = BITS == 8 ? (K + 1023) / 1024 : 1;
-  int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
-  s_want = s_want < s_min ? s_min : s_want;
-  s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
-  s_want = s_want > nkb ? nkb : s_want;
-  if (s_want < s_min)  // host checks keep K <= 16384 for int8
-    return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: K=%d needs %d-way split", K, s_min);
-  // the largest split whose clusters are all resident at once (one wave);
-  // the smallest allowed one if none is
-  int S = 0, NS = 0, rows_per = 0;
-  uint32_t a_col = 0, cols = 0;
-  size_t dyn = 0;
-  for (int s_try = s_want; s_try >= s_min; --s_try) {
-    const int per_cta = (nkb + s_try - 1) / s_try;
-    // stages: up to 6 within the shared-memory limit, no more than the
-    // k-blocks a CTA runs, and enough that the int32 partial tile of the
-    // split-K epilogue ([bt][128] int32) fits over them
-    const int ns_min = (int)(((size_t)bt * kTileN * 4 + stage_bytes(bt) - 1) / stage_bytes(bt));
-    int ns = per_cta > 6 ? 6 : per_cta;
-    if (ns < ns_min) ns = ns_min;
-    if (ns < 2) ns = 2;
-    while (ns > ns_min && ns > 2 && smem_bytes(bt, ns) > (size_t)kMaxSmem) --ns;
-    // tensor memory: accumulator [0, bt) then one 32-column A slot per stage
-    const uint32_t ac = (uint32_t)((bt + 31) / 32 * 32);
-    uint32_t c = 32;
-    while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
-    if (c > 512 || smem_bytes(bt, ns) > (size_t)kMaxSmem) continue;
-    // never more CTAs on an SM than its 512 tensor-memory columns hold: a CTA
-    // blocked in tcgen05.alloc while its cluster peers wait for it could
-    // otherwise wait on CTAs of another cluster in the same state
-    size_t d = smem_bytes(bt, ns);
-    const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
-    if (d < dyn_floor) d = dyn_floor;
-    S = s_try; NS = ns; a_col = ac; cols = c; dyn = d;
-    rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
-    const int active = vqlin::max_active_clusters((const void*)qgemm_kernel<BITS>, kThreads, d, s_try);
-    if (tiles_n * tiles_m <= active) break;
+
+  // One launch plan: token tile, K split, stages, tensor-memory columns and
+  // shared memory.  Returns false if no plan fits; `one_wave` tells whether
+  // all clusters are resident at once.
+  struct Plan {
+    bool chunked = false;
+    int bt = 0, tiles_n = 0, tiles_m = 0, S = 0, NS = 0, rows_per = 0;
+    uint32_t a_col = 0, cols = 0;
+    size_t dyn = 0;
+    bool one_wave = false;
+  };
+  // chunked: int8 beyond 1024 channels keeps two float32 accumulators and an
+  // int32 running sum in tensor memory (token tile <= 128); otherwise every
+  // CTA sums at most s_min-th of K (int8: <= 1024 channels)
+  auto make_plan = [&](bool chunked, int s_min, Plan& p) -> bool {
+    const int bt_max = chunked ? 128 : 256;
+    const int nt = (M + bt_max - 1) / bt_max;
+    const int bt = ((M + nt - 1) / nt + 15) / 16 * 16;
+    const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + bt - 1) / bt;
+    int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
+    s_want = s_want < s_min ? s_min : s_want;
+    s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
+    s_want = s_want > nkb ? nkb : s_want;
+    if (s_want < s_min) return false;
+    bool found = false;
+    // the largest split whose clusters are all resident at once (one wave);
+    // the smallest allowed one if none is
+    for (int s_try = s_want; s_try >= s_min; --s_try) {
+      const int per_cta = (nkb + s_try - 1) / s_try;
+      // stages: up to 6 within the shared-memory limit, no more than the
+      // k-blocks a CTA runs, and enough that the int32 partial tile of the
+      // split-K epilogue ([bt][128] int32) fits over them
+      const int ns_min = (int)(((size_t)bt * kTileN * 4 + stage_bytes(bt) - 1) / stage_bytes(bt));
+      // tensor memory: accumulator [0, bt) (chunking: two float32 accumulators
+      // and the int32 running sum), then one 32-column A slot per stage
+      const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
+      const uint32_t ac = chunked ? 3 * bt_pad : bt_pad;
+      const int ns_tmem = (int)((512 - ac) / kACols);
+      int ns = per_cta > 6 ? 6 : per_cta;
+      if (ns > ns_tmem) ns = ns_tmem;
+      if (ns < ns_min) ns = ns_min;
+      if (ns < 2) ns = 2;
+      while (ns > ns_min && ns > 2 && smem_bytes(bt, ns) > (size_t)kMaxSmem) --ns;
+      uint32_t c = 32;
+      while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
+      if (c > 512 || smem_bytes(bt, ns) > (size_t)kMaxSmem) continue;
+      // never more CTAs on an SM than its 512 tensor-memory columns hold: a
+      // CTA blocked in tcgen05.alloc while its cluster peers wait for it could
+      // otherwise wait on CTAs of another cluster in the same state
+      size_t d = smem_bytes(bt, ns);
+      const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
+      if (d < dyn_floor) d = dyn_floor;
+      p.chunked = chunked; p.bt = bt; p.tiles_n = tiles_n; p.tiles_m = tiles_m;
+      p.S = s_try; p.NS = ns; p.a_col = ac; p.cols = c; p.dyn = d;
+      p.rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+      found = true;
+      const int active = vqlin::max_active_clusters((const void*)qgemm_kernel<BITS>, kThreads, d, s_try);
+      p.one_wave = tiles_n * tiles_m <= active;
+      if (p.one_wave) break;
+    }
+    return found;
+  };
+  Plan plan;
+  bool have = false;
+  if (BITS == 8 && K > 1024) {
+    // int8: split K over a cluster so no CTA sums more than 1024 channels if
+    // that runs in one wave, else chunk inside each CTA
+    Plan split;
+    if (make_plan(false, (K + 1023) / 1024, split) && split.one_wave) {
+      plan = split;
+      have = true;
+    } else {
+      have = make_plan(true, 1, plan);
+    }
+  } else {
+    have = make_plan(false, 1, plan);
   }
-  if (S == 0) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: no tile plan for M=%d N=%d K=%d", M, N, K);
+  if (!have) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: no tile plan for M=%d N=%d K=%d", M, N, K);
+  const bool chunked = plan.chunked;
+  const int bt = plan.bt, tiles_n = plan.tiles_n, tiles_m = plan.tiles_m, S = plan.S, NS = plan.NS;
+  const int rows_per = plan.rows_per;
+  const uint32_t a_col = plan.a_col, cols = plan.cols;
+  const size_t dyn = plan.dyn;
   const bool tma_store = S == 1 && acc == nullptr && (N % 8) == 0;
 
   CUtensorMap tmW, tmX, tmY;
@@ -502,6 +618,12 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   QgemmArgs a;
   a.sx = sx; a.sw = sw; a.bias = bias; a.Y = Y; a.acc = acc; a.status = status;
   a.M = M; a.N = N; a.K = K; a.bt = bt; a.nkb = nkb; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
+  {
+    const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
+    a.chunk_kb = chunked ? 1024 / kb_codes : 0;
+    a.d1_col = bt_pad;
+    a.r_col = 2 * bt_pad;
+  }
   a.wait_limit_ns = limit_ns; a.withhold_loads = withhold;
   a.tma_store = tma_store ? 1 : 0; a.rows_per = rows_per;
 

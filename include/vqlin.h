@@ -143,9 +143,9 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
                                int M, int N, int K, void* stream);
 
 /* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
- * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands; at
- * most 1024 channels per float32 partial sum, which bounds it below 2^24).
- * Requires K % 64 == 0 and K <= 16384. */
+ * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands;
+ * float32 partial sums cover at most 1024 channels, which bounds them below
+ * 2^24, and are added up in int32).  Requires K % 64 == 0 and K <= 65536. */
 vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq,
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);

@@ -217,15 +217,13 @@ def test_weight_quant_asymmetric_bit_exact(group, NK):
 GEMM_SHAPES = [(1, 8, 256), (16, 256, 256), (17, 200, 384), (50, 1024, 1024), (129, 257, 512),
                (128, 128, 2048), (816, 256, 2048), (64, 4096, 128), (3, 11008, 256),
                (50, 1024, 4096), (257, 136, 1024), (512, 384, 2048), (64, 256, 16384),
-               (816, 2560, 2048), (33, 1000, 11008)]
+               (816, 2560, 2048), (33, 1000, 11008), (816, 512, 16384), (300, 384, 4096), (2, 128, 32768)]
 
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("shape", GEMM_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_int_gemm_bit_exact(bits, shape):
     M, N, K = shape
-    if bits == 8 and K > 16384:
-        pytest.skip("int8 GEMM supports K <= 16384")
     qmax = 7 if bits == 4 else 127
     xq = random_codes((M, K), -qmax, qmax, seed=1, tags=("x", bits))
     wq = random_codes((N, K), -qmax, qmax, seed=2, tags=("w", bits))
@@ -237,8 +235,12 @@ def test_int_gemm_bit_exact(bits, shape):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-def test_int_gemm_extremes(bits):
-    M, N, K = 4, 16, 16384
+@pytest.mark.parametrize("K", [16384, 65536])
+def test_int_gemm_extremes(bits, K):
+    # all-maximum codes: the int8 sum reaches 127^2 K (2^30 at K = 65536), far
+    # beyond the 2^24 float32 range, so it is exact only through the chunked
+    # int32 accumulation
+    M, N = 4, 16
     qmax = 7 if bits == 4 else 127
     xq = np.full((M, K), -qmax, np.int8)
     wq = np.full((N, K), -qmax, np.int8)
