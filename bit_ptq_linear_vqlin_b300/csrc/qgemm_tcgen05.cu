@@ -175,13 +175,34 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     // bias (float) while lane 0 produces; the epilogue waits on scl_ready
     if (lane > 0) {
       if (a.acc == nullptr) {
-        for (int i = lane - 1; i < kTileN; i += 31) {
-          const bool in = n0 + i < a.N;
-          s_sw[i] = in ? __ldg(a.sw + n0 + i) : 0.0f;
-          s_bias[i] = in && a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n0 + i) << 16) : 0.0f;
+        // every load of a lane is issued before any is used (one latency)
+        float wv[5], bv[5], xv[9];
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+          const int i = lane - 1 + 31 * j;
+          const bool in = i < kTileN && n0 + i < a.N;
+          wv[j] = in ? __ldg(a.sw + n0 + i) : 0.0f;
+          bv[j] = in && a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n0 + i) << 16) : 0.0f;
         }
         pdl_wait();  // the per-token scales come from the previous kernel
-        for (int i = lane - 1; i < bt; i += 31) s_sx[i] = m0 + i < a.M ? __ldg(a.sx + m0 + i) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const int i = lane - 1 + 31 * j;
+          xv[j] = i < bt && m0 + i < a.M ? __ldg(a.sx + m0 + i) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+          const int i = lane - 1 + 31 * j;
+          if (i < kTileN) {
+            s_sw[i] = wv[j];
+            s_bias[i] = bv[j];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const int i = lane - 1 + 31 * j;
+          if (i < bt) s_sx[i] = xv[j];
+        }
       }
       mbar_arrive(scl_ready);
     }
