@@ -223,9 +223,10 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           tma_load_2d(base + (size_t)i * stage_bytes, &tmX, (kb0 + i) * kXStep, m0, &full[i]);
           ++issued;
         }
+        int s = 0;        // stage of k-block i
+        uint32_t ph = 0;  // parity of the release of stage s that k-block i waits for
         for (int i = pre; i < cnt; ++i) {
-          const int s = i % NS;
-          if (!mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, a.wait_limit_ns, abort)) {
+          if (!mbar_wait_bounded(&empty[s], ph, a.wait_limit_ns, abort)) {
             if (!*abort) record_timeout(a.status, abort);
             break;
           }
@@ -234,6 +235,10 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           tma_load_2d(st + b_bytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
           tma_load_2d(st, &tmX, (kb0 + i) * kXStep, m0, &full[s]);
           ++issued;
+          if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       } else {
         pdl_wait();
@@ -248,33 +253,53 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     if (lane == 0) {
       const uint32_t id = idesc_f32acc(0u, kTileN, bt);  // e4m3 x e4m3 or f16 x f16 -> f32
       const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
+      // the issue loop is kept short: one thread must issue an MMA about every
+      // 64 cycles to keep the tensor core busy, so stage, phase, chunk and
+      // descriptors advance incrementally (no divisions)
+      const uint64_t db0 = sdesc_sw128(base);
+      const uint64_t dstep = (uint64_t)(stage_bytes >> 4);  // start-address field step per stage
+      const uint32_t ta0 = tmem + a.a_col;
+      int s = 0, kin = 0, c = 0;  // stage; k-block inside the chunk; chunk
+      uint32_t ph = 0;            // phase parity of stage s
       for (int i = 0; i < cnt; ++i) {
-        const int s = i % NS;
         // chunking: chunk c accumulates into float32 buffer c & 1, which the
         // expanders drain into the int32 running sum before chunk c + 2 reuses it
-        const int ckd = ck > 0 ? ck : 1;
-        const int c = ck ? i / ckd : 0, kin = ck ? i % ckd : i;
         const uint32_t dacc = tmem + ((c & 1) ? a.d1_col : 0u);
         if (ck && kin == 0 && c >= 2 &&
             !mbar_wait_bounded(&acce[c & 1], ((c >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
-        if (!mbar_wait_bounded(&aready[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
+        if (!mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
         tc_fence_after();
-        const uint64_t db = sdesc_sw128(base + (size_t)s * stage_bytes);
-        const uint32_t ta = tmem + a.a_col + (uint32_t)(s * kACols);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // per MMA: 8 tensor-memory columns of A, 32 bytes along the swizzled B row
-          if (BITS == 4) mma_f8f6f4_ta(dacc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
-          else mma_f16_ta(dacc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
+        const uint64_t db = db0 + (uint64_t)s * dstep;
+        const uint32_t ta = ta0 + (uint32_t)(s * kACols);
+        // per MMA: 8 tensor-memory columns of A, 32 bytes along the swizzled B row
+        if (BITS == 4) {
+          mma_f8f6f4_ta(dacc, ta, db, id, kin != 0 ? 1u : 0u);
+          mma_f8f6f4_ta(dacc, ta + 8, db + 2, id, 1u);
+          mma_f8f6f4_ta(dacc, ta + 16, db + 4, id, 1u);
+          mma_f8f6f4_ta(dacc, ta + 24, db + 6, id, 1u);
+        } else {
+          mma_f16_ta(dacc, ta, db, id, kin != 0 ? 1u : 0u);
+          mma_f16_ta(dacc, ta + 8, db + 2, id, 1u);
+          mma_f16_ta(dacc, ta + 16, db + 4, id, 1u);
+          mma_f16_ta(dacc, ta + 24, db + 6, id, 1u);
         }
         tc_commit(&empty[s]);
-        if (ck && (kin == ck - 1 || i == cnt - 1)) tc_commit(&accf[c & 1]);
+        ++kin;
+        if (ck && (kin == ck || i == cnt - 1)) {
+          tc_commit(&accf[c & 1]);
+          kin = 0;
+          ++c;
+        }
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       tc_commit(acc_full);
     }
@@ -316,9 +341,10 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       return true;
     };
     bool ok_all = true;
+    int s = 0, kin = 0, c = 0;  // stage; k-block inside the chunk; chunk
+    uint32_t ph = 0;            // phase parity of stage s
     for (int i = 0; i < cnt; ++i) {
-      const int s = i % NS;
-      const bool ok = mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort);
+      const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
@@ -336,13 +362,22 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aready[s]);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
       if (ck > 0) {
-        const int ckd = ck > 0 ? ck : 1;  // (a divisor the compiler sees as non-zero)
-        if (i >= ckd && i % ckd == 0 && !drain(i / ckd - 1)) {
+        // after the first k-block of chunk c, drain chunk c - 1; the last
+        // chunk is drained after the last k-block
+        if (c > 0 && kin == 0 && !drain(c - 1)) {
           ok_all = false;
           break;
         }
-        if (i == cnt - 1 && !drain(i / ckd)) ok_all = false;
+        if (i == cnt - 1 && !drain(c)) ok_all = false;
+        if (++kin == ck) {
+          kin = 0;
+          ++c;
+        }
       }
     }
     (void)ok_all;

@@ -166,9 +166,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         tma_load_2d(base + (size_t)i * kStageBytes, &tmX, (kb0 + i) * kKB, m0, &full[i]);
         ++issued;
       }
+      int s = 0;        // stage of k-block i
+      uint32_t ph = 0;  // parity of the release of stage s that k-block i waits for
       for (int i = pre; i < cnt; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait_bounded(&empty[s], ((i / NS) - 1) & 1, a.wait_limit_ns, abort)) {
+        if (!mbar_wait_bounded(&empty[s], ph, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
@@ -177,6 +178,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         tma_load_2d(st + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
         tma_load_2d(st, &tmX, (kb0 + i) * kKB, m0, &full[s]);
         ++issued;
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
         if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
@@ -186,26 +191,40 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
+      // stage, phase and group advance incrementally so the single issuing
+      // thread spends as few cycles as possible between MMAs
+      const uint64_t db0 = sdesc_sw128(base);
+      const uint32_t ta0 = tmem + a.a_col;
+      int s = 0, kin = 0, jl = 0;  // stage; k-block inside the group; local group
+      uint32_t ph = 0;             // phase parity of stage s
       for (int i = 0; i < cnt; ++i) {
-        const int s = i % NS;
-        const int jl = i / KB_PER_G, kin = i % KB_PER_G;  // local group, k-block inside it
         const uint32_t acc = tmem + (uint32_t)((jl & 1) * BT);
         if (kin == 0 && jl >= 2 &&
             !mbar_wait_bounded(&acce[jl & 1], ((jl >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
-        if (!mbar_wait_bounded(&aready[s], (i / NS) & 1, a.wait_limit_ns, abort)) {
+        if (!mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort)) {
           if (!*abort) record_timeout(a.status, abort);
           break;
         }
         tc_fence_after();
-        const uint64_t db = sdesc_sw128(base + (size_t)s * kStageBytes);
-        const uint32_t ta = tmem + a.a_col + (uint32_t)(s * kACols);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_f16_ta(acc, ta + 8 * j, db + 2 * j, id, (kin | j) != 0);
+        const uint64_t db = db0 + (uint64_t)(s * (kStageBytes >> 4));
+        const uint32_t ta = ta0 + (uint32_t)(s * kACols);
+        mma_f16_ta(acc, ta, db, id, kin != 0 ? 1u : 0u);
+        mma_f16_ta(acc, ta + 8, db + 2, id, 1u);
+        mma_f16_ta(acc, ta + 16, db + 4, id, 1u);
+        mma_f16_ta(acc, ta + 24, db + 6, id, 1u);
         tc_commit(&empty[s]);
-        if (kin == KB_PER_G - 1) tc_commit(&accf[jl & 1]);
+        if (++kin == KB_PER_G) {
+          tc_commit(&accf[jl & 1]);
+          kin = 0;
+          ++jl;
+        }
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       tc_commit(done);  // tensor memory is freed only after this completes
     }
@@ -219,9 +238,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col + (uint32_t)(16 * h);
     uint32_t zz = ng > 0 ? zero_pair(a, n, g0) : 0u;
     uint32_t zz_next = ng > 1 ? zero_pair(a, n, g0 + 1) : 0u;
+    int s = 0, kin = 0, jl = 0;  // stage; k-block inside the group; local group
+    uint32_t ph = 0;             // phase parity of stage s
     for (int i = 0; i < cnt; ++i) {
-      const int s = i % NS;
-      const bool ok = mbar_wait_bounded(&full[s], (i / NS) & 1, a.wait_limit_ns, abort);
+      const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
@@ -238,10 +258,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aready[s]);
-      if (i % KB_PER_G == KB_PER_G - 1) {  // next group: rotate the zero points
-        const int jn = i / KB_PER_G + 2;
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+      if (++kin == KB_PER_G) {  // next group: rotate the zero points
+        kin = 0;
+        ++jl;
         zz = zz_next;
-        zz_next = jn < ng ? zero_pair(a, n, g0 + jn) : 0u;
+        zz_next = jl + 1 < ng ? zero_pair(a, n, g0 + jl + 1) : 0u;
       }
     }
   } else {
