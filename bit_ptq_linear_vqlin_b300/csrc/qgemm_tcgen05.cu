@@ -121,7 +121,8 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_sx[256], s_sw[kTileN], s_bias[kTileN];
+  __shared__ __align__(16) float s_sx[256];
+  __shared__ float s_sw[kTileN], s_bias[kTileN];
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int bt = a.bt;
@@ -136,6 +137,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   uint64_t* scl_ready = acc_full + 1;
   uint64_t* accf = acc_full + 2;       // [2] chunking: MMA -> drain (chunk accumulated)
   uint64_t* acce = acc_full + 4;       // [2] chunking: drain -> MMA (accumulator free)
+  uint64_t* red_full = acc_full + 6;   // split K: the peers' partial slices added in
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z;
@@ -150,7 +152,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     s_abort = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&aready[i], kExpandWarps);
+      mbar_init(&aready[i], kExpandWarps / 2);  // one group of four warps per k-block
       mbar_init(&empty[i], 1);
     }
     mbar_init(acc_full, 1);
@@ -159,6 +161,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       mbar_init(&accf[i], 1);
       mbar_init(&acce[i], kExpandWarps);
     }
+    mbar_init(red_full, 1);
     mbar_init_fence();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -198,10 +201,16 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
             s_bias[i] = bv[j];
           }
         }
+        // token scales in the unit of the epilogue's accumulator value: float32
+        // sums of int4 (int8) products are integers x 2^-18 (2^-48), scaled here
+        // by 2^18 (2^48) once instead of per element; chunked int8 sums and all
+        // split-K sums reach the epilogue as int32
+        const float su = (S == 1 && (BITS == 4 || a.chunk_kb == 0)) ? (BITS == 4 ? 262144.0f : 281474976710656.0f)
+                                                                      : 1.0f;
 #pragma unroll
         for (int j = 0; j < 9; ++j) {
           const int i = lane - 1 + 31 * j;
-          if (i < bt) s_sx[i] = xv[j];
+          if (i < bt) s_sx[i] = xv[j] * su;
         }
       }
       mbar_arrive(scl_ready);
@@ -250,12 +259,13 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop (warp-uniform control flow, every wait
+    // decided by a vote) and one elected lane issues each MMA and commit: a
+    // single lane looping in a diverged warp issues MMAs too slowly to keep
+    // the tensor core busy
+    {
       const uint32_t id = idesc_f32acc(0u, kTileN, bt);  // e4m3 x e4m3 or f16 x f16 -> f32
       const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
-      // the issue loop is kept short: one thread must issue an MMA about every
-      // 64 cycles to keep the tensor core busy, so stage, phase, chunk and
-      // descriptors advance incrementally (no divisions)
       const uint64_t db0 = sdesc_sw128(base);
       const uint64_t dstep = (uint64_t)(stage_bytes >> 4);  // start-address field step per stage
       const uint32_t ta0 = tmem + a.a_col;
@@ -265,13 +275,16 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         // chunking: chunk c accumulates into float32 buffer c & 1, which the
         // expanders drain into the int32 running sum before chunk c + 2 reuses it
         const uint32_t dacc = tmem + ((c & 1) ? a.d1_col : 0u);
-        if (ck && kin == 0 && c >= 2 &&
-            !mbar_wait_bounded(&acce[c & 1], ((c >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
-          if (!*abort) record_timeout(a.status, abort);
-          break;
+        if (ck && kin == 0 && c >= 2) {
+          const bool ok = mbar_wait_bounded(&acce[c & 1], ((c >> 1) - 1) & 1, a.wait_limit_ns, abort);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (!ok && !*abort) record_timeout(a.status, abort);
+            break;
+          }
         }
-        if (!mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort)) {
-          if (!*abort) record_timeout(a.status, abort);
+        const bool ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (!ok && !*abort) record_timeout(a.status, abort);
           break;
         }
         tc_fence_after();
@@ -279,20 +292,20 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         const uint32_t ta = ta0 + (uint32_t)(s * kACols);
         // per MMA: 8 tensor-memory columns of A, 32 bytes along the swizzled B row
         if (BITS == 4) {
-          mma_f8f6f4_ta(dacc, ta, db, id, kin != 0 ? 1u : 0u);
-          mma_f8f6f4_ta(dacc, ta + 8, db + 2, id, 1u);
-          mma_f8f6f4_ta(dacc, ta + 16, db + 4, id, 1u);
-          mma_f8f6f4_ta(dacc, ta + 24, db + 6, id, 1u);
+          mma_f8f6f4_ta_warp(dacc, ta, db, id, kin != 0 ? 1u : 0u);
+          mma_f8f6f4_ta_warp(dacc, ta + 8, db + 2, id, 1u);
+          mma_f8f6f4_ta_warp(dacc, ta + 16, db + 4, id, 1u);
+          mma_f8f6f4_ta_warp(dacc, ta + 24, db + 6, id, 1u);
         } else {
-          mma_f16_ta(dacc, ta, db, id, kin != 0 ? 1u : 0u);
-          mma_f16_ta(dacc, ta + 8, db + 2, id, 1u);
-          mma_f16_ta(dacc, ta + 16, db + 4, id, 1u);
-          mma_f16_ta(dacc, ta + 24, db + 6, id, 1u);
+          mma_f16_ta_warp(dacc, ta, db, id, kin != 0 ? 1u : 0u);
+          mma_f16_ta_warp(dacc, ta + 8, db + 2, id, 1u);
+          mma_f16_ta_warp(dacc, ta + 16, db + 4, id, 1u);
+          mma_f16_ta_warp(dacc, ta + 24, db + 6, id, 1u);
         }
-        tc_commit(&empty[s]);
+        tc_commit_warp(&empty[s]);
         ++kin;
         if (ck && (kin == ck || i == cnt - 1)) {
-          tc_commit(&accf[c & 1]);
+          tc_commit_warp(&accf[c & 1]);
           kin = 0;
           ++c;
         }
@@ -301,21 +314,22 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           ph ^= 1u;
         }
       }
-      tc_commit(acc_full);
+      tc_commit_warp(acc_full);
     }
   } else {
     // ------------------------------------------------- weight expanders (2..9)
     // thread = weight row (its warp's tensor-memory lane quadrant); the two
-    // warps of a quadrant take the two 32-byte halves of the 64-byte row
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    // groups of four warps take alternate k-blocks, so one group's tensor
+    // memory stores are in flight while the other group expands
+    const int q = warp & 3, g = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const int sw = (row >> 1) & 3;  // 64-byte swizzle of the packed tile
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t trow = lanes + a.a_col + (uint32_t)(16 * h);
+    const uint32_t trow = lanes + a.a_col;
     const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
     const float unit = 281474976710656.0f;  // 2^48: f16-operand accumulator -> integer
     // chunking: adds float32 chunk c (exact integers x 2^-48, each below 2^24)
-    // into the int32 running sum; this warp takes columns 16h, 16h + 32, ...
+    // into the int32 running sum; group g takes columns 16g, 16g + 32, ...
     auto drain = [&](int c) -> bool {
       const bool okc = mbar_wait_bounded(&accf[c & 1], (c >> 1) & 1, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, okc)) {
@@ -324,15 +338,24 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       }
       tc_fence_after();
       const uint32_t src = lanes + ((c & 1) ? a.d1_col : 0u);
-      for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-        uint32_t v[16], r[16];
-        tmem_ld_x16(src + (uint32_t)c0, v);
-        if (c > 0) tmem_ld_x16(lanes + a.r_col + (uint32_t)c0, r);
+      for (int cb = 16 * g; cb < bt; cb += 64) {
+        const bool two = cb + 32 < bt;  // warp-uniform
+        uint32_t v[2][16], r[2][16];
+        tmem_ld_x16(src + (uint32_t)cb, v[0]);
+        if (two) tmem_ld_x16(src + (uint32_t)(cb + 32), v[1]);
+        if (c > 0) {
+          tmem_ld_x16(lanes + a.r_col + (uint32_t)cb, r[0]);
+          if (two) tmem_ld_x16(lanes + a.r_col + (uint32_t)(cb + 32), r[1]);
+        }
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          r[j] = (uint32_t)((c > 0 ? (int32_t)r[j] : 0) + __float2int_rn(__uint_as_float(v[j]) * unit));
-        tmem_st_x16(lanes + a.r_col + (uint32_t)c0, r);
+        for (int u = 0; u < 2; ++u) {
+          if (u == 1 && !two) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            r[u][j] = (uint32_t)((c > 0 ? (int32_t)r[u][j] : 0) + __float2int_rn(__uint_as_float(v[u][j]) * unit));
+          tmem_st_x16(lanes + a.r_col + (uint32_t)(cb + 32 * u), r[u]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -341,50 +364,68 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       return true;
     };
     bool ok_all = true;
-    int s = 0, kin = 0, c = 0;  // stage; k-block inside the chunk; chunk
-    uint32_t ph = 0;            // phase parity of stage s
-    for (int i = 0; i < cnt; ++i) {
+    int s = g, kin = g, c = 0, drained = 0;  // stage; k-block inside chunk c; chunks drained
+    uint32_t ph = 0;                          // phase parity of stage s
+    if (ck > 0)
+      while (kin >= ck) {
+        kin -= ck;
+        ++c;
+      }
+    for (int i = g; i < cnt; i += 2) {
       const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
+        ok_all = false;
         break;
       }
       const uint8_t* rawrow = base + (size_t)s * stage_bytes + b_bytes + row * kRawRow;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(rawrow + (((2 * h) ^ sw) << 4));
-      const uint4 c1 = *reinterpret_cast<const uint4*>(rawrow + (((2 * h + 1) ^ sw) << 4));
-      uint32_t v[16];
-      expand8<BITS>(c0.x, c0.y, v);
-      expand8<BITS>(c0.z, c0.w, v + 4);
-      expand8<BITS>(c1.x, c1.y, v + 8);
-      expand8<BITS>(c1.z, c1.w, v + 12);
-      tmem_st_x16(trow + (uint32_t)(s * kACols), v);
+      uint4 rw[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) rw[j] = *reinterpret_cast<const uint4*>(rawrow + ((j ^ sw) << 4));
+      uint32_t v[2][16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        expand8<BITS>(rw[j].x, rw[j].y, &v[j >> 1][8 * (j & 1)]);
+        expand8<BITS>(rw[j].z, rw[j].w, &v[j >> 1][8 * (j & 1) + 4]);
+      }
+      const uint32_t ta = trow + (uint32_t)(s * kACols);
+      tmem_st_x16(ta, v[0]);
+      tmem_st_x16(ta + 16, v[1]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aready[s]);
-      if (++s == NS) {
-        s = 0;
+      s += 2;
+      if (s >= NS) {
+        s -= NS;
         ph ^= 1u;
       }
       if (ck > 0) {
-        // after the first k-block of chunk c, drain chunk c - 1; the last
-        // chunk is drained after the last k-block
-        if (c > 0 && kin == 0 && !drain(c - 1)) {
-          ok_all = false;
-          break;
-        }
-        if (i == cnt - 1 && !drain(c)) ok_all = false;
-        if (++kin == ck) {
-          kin = 0;
+        // chunks before the one of this k-block are complete: drain them
+        while (drained < c)
+          if (!drain(drained++)) {
+            ok_all = false;
+            break;
+          }
+        if (!ok_all) break;
+        kin += 2;
+        while (kin >= ck) {
+          kin -= ck;
           ++c;
         }
       }
+    }
+    if (ck > 0 && ok_all && cnt > 0) {
+      const int c_last = (cnt - 1) / (ck > 0 ? ck : 1);  // (a divisor the compiler sees as non-zero)
+      while (drained <= c_last)
+        if (!drain(drained++)) break;
     }
     (void)ok_all;
   }
 
   // ---------------------------------------------------------------- epilogue
   __syncwarp();  // the single-thread roles rejoin their warps
+  const bool chunked = BITS == 8 && a.chunk_kb > 0;
   const float unit = BITS == 4 ? 262144.0f : 281474976710656.0f;  // 2^18, 2^48: accumulator -> integer
   const bool raw_out = a.acc != nullptr;
   bool go = false;
@@ -397,26 +438,26 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     go = __all_sync(0xffffffffu, ok && !*abort);
   }
   pdl_wait();  // global writes only once the previous kernel has finished
-  // warps 2..9: lane quadrant q of tensor memory, 16-column chunks h, h+2, ...
+  // warps 2..9: lane quadrant q of tensor memory, 16-column chunks 16h + 32k
   const int q = warp & 3;
   const int h = (warp - 2) >> 2;
-  const int row = q * 32 + lane;   // output channel inside the tile
-  // 16 int32 accumulators of this thread's row, columns c0 .. c0 + 15
-  auto load_acc = [&](int c0, int32_t (&out)[16]) {
-    uint32_t v[16];
-    const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-    if (BITS == 8 && a.chunk_kb) {
-      tmem_ld_x16(lanes + a.r_col + (uint32_t)c0, v);
-      tmem_ld_wait();
+  const int row = q * 32 + lane;  // output channel inside the tile
+  const uint32_t lanes_q = tmem + ((uint32_t)(q * 32) << 16);
+  // accumulator words of this thread's row in columns cb + 32u .. + 15, for
+  // the u < 4 with cb + 32u < bt: four tensor-memory loads, one wait
+  auto load4 = [&](int cb, uint32_t (&v)[4][16]) {
+    const uint32_t src = lanes_q + (chunked ? a.r_col : 0u) + (uint32_t)cb;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) out[j] = (int32_t)v[j];
-    } else {
-      tmem_ld_x16(lanes + (uint32_t)c0, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) out[j] = __float2int_rn(__uint_as_float(v[j]) * unit);
-    }
+    for (int u = 0; u < 4; ++u)
+      if (cb + 32 * u < bt) tmem_ld_x16(src + (uint32_t)(32 * u), v[u]);  // warp-uniform
+    tmem_ld_wait();
   };
+  // the exact integer sum held by an accumulator word
+  auto as_int = [&](uint32_t w) -> int32_t {
+    return chunked ? (int32_t)w : __float2int_rn(__uint_as_float(w) * unit);
+  };
+  // the same sum as a float in the unit of s_sx (see the staging above)
+  auto as_f = [&](uint32_t w) -> float { return chunked ? (float)(int32_t)w : __uint_as_float(w); };
 
   if (S == 1 && a.tma_store) {
     // bf16 tile [bt tokens][128 channels] staged over the idle stages, then one
@@ -425,14 +466,26 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     if (warp >= 2) {
       if (go) {
         const float sw_n = s_sw[row], b_n = s_bias[row];
-        for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-          int32_t v[16];
-          load_acc(c0, v);
+        for (int cb = 16 * h; cb < bt; cb += 128) {
+          uint32_t v[4][16];
+          load4(cb, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float acc = (float)v[j];
-            ystage[(c0 + j) * kTileN + row] =
-                f32_to_bf16_rn(__fadd_rn(__fmul_rn(__fmul_rn(acc, s_sx[c0 + j]), sw_n), b_n));
+          for (int u = 0; u < 4; ++u) {
+            const int c0 = cb + 32 * u;
+            if (c0 >= bt) break;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 sx4 = *reinterpret_cast<const float4*>(&s_sx[c0 + j]);  // 4 token scales
+              // two tokens of this channel per paired conversion to bf16
+              const uint32_t p0 = pack_bf16x2_rn(fmaf(as_f(v[u][j]) * sx4.x, sw_n, b_n),
+                                                 fmaf(as_f(v[u][j + 1]) * sx4.y, sw_n, b_n));
+              const uint32_t p1 = pack_bf16x2_rn(fmaf(as_f(v[u][j + 2]) * sx4.z, sw_n, b_n),
+                                                 fmaf(as_f(v[u][j + 3]) * sx4.w, sw_n, b_n));
+              ystage[(c0 + j) * kTileN + row] = (uint16_t)p0;
+              ystage[(c0 + j + 1) * kTileN + row] = (uint16_t)(p0 >> 16);
+              ystage[(c0 + j + 2) * kTileN + row] = (uint16_t)p1;
+              ystage[(c0 + j + 3) * kTileN + row] = (uint16_t)(p1 >> 16);
+            }
           }
         }
         fence_proxy_async_smem();
@@ -452,21 +505,22 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     if (warp >= 2 && go) {
       const int n = n0 + row;
       const float sw_n = s_sw[row], b_n = s_bias[row];
-      for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-        int32_t v[16];
-        load_acc(c0, v);
-        if (n < a.N) {
+      for (int cb = 16 * h; cb < bt; cb += 128) {
+        uint32_t v[4][16];
+        load4(cb, v);
+        if (n >= a.N) continue;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c0 = cb + 32 * u;
+          if (c0 >= bt) break;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
             if (m < a.M) {
-              const int32_t acc = v[j];
-              if (raw_out) {
-                a.acc[(size_t)m * a.N + n] = acc;
-              } else {
-                const float y = __fadd_rn(__fmul_rn(__fmul_rn((float)acc, s_sx[c0 + j]), sw_n), b_n);
-                a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(y);
-              }
+              if (raw_out)
+                a.acc[(size_t)m * a.N + n] = as_int(v[u][j]);
+              else
+                a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(fmaf(as_f(v[u][j]) * s_sx[c0 + j], sw_n, b_n));
             }
           }
         }
@@ -475,66 +529,102 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
   } else {
-    // split K: int32 partial tile part[token][channel] in this CTA's shared
-    // memory (it overlays the idle stages); after a cluster barrier, CTA r of
-    // the cluster sums channels [r0, r0 + rows_per) over all S partials with
-    // 16-byte DSMEM loads and writes them out.
-    int32_t* part = reinterpret_cast<int32_t*>(base);
+    // split K, reduce-scatter over the cluster: cluster rank r owns output
+    // channels [r rp, (r + 1) rp).  Every CTA writes its 32-bit partial tile as
+    // S slices part[r][token][rp] (over the idle stages; int4 and int8 sums as
+    // int32), then adds slice r into rank r's slice with one bulk reduction
+    // each; rank r scales and stores its slice once all S - 1 have landed.
+    const int rp = a.rows_per;
+    const uint32_t slice_words = (uint32_t)(bt * rp);
+    const uint32_t slice_bytes = slice_words * 4u;
+    const int own0 = (int)rank * rp;                                     // first owned channel
+    const int own_n = own0 < kTileN ? min(rp, kTileN - own0) : 0;        // channels owned here
+    uint32_t* part = reinterpret_cast<uint32_t*>(base);
+    if (tid == 64 && own_n > 0) mbar_arrive_expect_tx(red_full, (uint32_t)(S - 1) * slice_bytes);
     if (warp >= 2 && go) {
-      for (int c0 = 16 * h; c0 < bt; c0 += 32) {
-        int32_t v[16];
-        load_acc(c0, v);
+      const int sl = row / rp, k = row - sl * rp;
+      uint32_t* dst = part + (size_t)sl * slice_words + k;
+      for (int cb = 16 * h; cb < bt; cb += 128) {
+        uint32_t v[4][16];
+        load4(cb, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) part[(c0 + j) * kTileN + row] = v[j];
+        for (int u = 0; u < 4; ++u) {
+          const int c0 = cb + 32 * u;
+          if (c0 >= bt) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            uint32_t w;
+            if (BITS == 4) {
+              // |sum| < 2^22: the integer sits in the low mantissa bits of
+              // sum + 1.5 x 2^23 (exact), no conversion instruction needed
+              w = (uint32_t)(__float_as_int(fmaf(__uint_as_float(v[u][j]), unit, 12582912.0f)) - 0x4B400000);
+            } else {
+              w = (uint32_t)as_int(v[u][j]);
+            }
+            dst[(size_t)(c0 + j) * rp] = w;
+          }
+        }
       }
+      fence_proxy_async_smem();  // the bulk reductions read and write these words
     }
     tc_fence_before();
-    cluster_sync_all();
-    if (!*abort) {
-      const int rows_per = a.rows_per;
-      const int r0 = (int)rank * rows_per;
-      const int nq = (min(kTileN, r0 + rows_per) - r0) / 4;  // 4-channel groups owned here
-      const uint32_t part_s = smem_addr(part);
+    __syncwarp();
+    cluster_sync_all();  // every CTA's partial slices are in place
+    // the slices are sent even after an abort (their contents are then
+    // meaningless), so every bulk reduction completes before any CTA exits
+    const uint32_t part_s = smem_addr(part);
+    if (tid >= 64 && tid < 64 + S) {
+      const int r = tid - 64;
+      if (r != (int)rank && r * rp < kTileN) {
+        const uint32_t off = (uint32_t)r * slice_bytes;
+        bulk_reduce_add_u32_to_peer(mapa_shared(part_s + off, (uint32_t)r), part_s + off, slice_bytes,
+                                    mapa_shared(smem_addr(red_full), (uint32_t)r));
+      }
+    }
+    bool got = true;
+    if (own_n > 0) {
+      got = mbar_wait_bounded(red_full, 0, a.wait_limit_ns, nullptr);
+      if (!got) record_timeout(a.status, abort);
+    }
+    got = got && own_n > 0 && !*abort;
+    // this CTA has all it receives: once every rank has arrived here, no
+    // bulk reduction reads or writes any of the cluster's shared memory
+    __syncwarp();
+    cluster_arrive();
+    if (got) {
+      const int nq = own_n / 4;  // 4-channel groups owned here
+      const int total = nq * bt;
       const bool vec = (a.N & 3) == 0;
-      for (int idx = tid; idx < nq * bt; idx += kThreads) {
-        const int rr = r0 + 4 * (idx % nq), col = idx / nq;
-        const int m = m0 + col, n = n0 + rr;
+      const uint32_t* mine = part + (size_t)rank * slice_words;
+      for (int idx = tid; idx < total; idx += kThreads) {
+        const int c = idx / nq, k = 4 * (idx - (idx / nq) * nq);
+        const int m = m0 + c, rr = own0 + k, n = n0 + rr;
         if (m >= a.M || n >= a.N) continue;
-        const uint32_t off = (uint32_t)(col * kTileN + rr) * 4u;
-        int4 pv[kMaxSplit];
-#pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c)
-          if (c < S) pv[c] = ld_shared_cluster_v4(mapa_shared(part_s + off, (uint32_t)c));
-        int32_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int c = 0; c < kMaxSplit; ++c)
-          if (c < S) {
-            acc[0] += pv[c].x; acc[1] += pv[c].y; acc[2] += pv[c].z; acc[3] += pv[c].w;
-          }
+        const uint4 t = *reinterpret_cast<const uint4*>(mine + (size_t)c * rp + k);
+        const int32_t acc[4] = {(int32_t)t.x, (int32_t)t.y, (int32_t)t.z, (int32_t)t.w};
         if (raw_out) {
-          int32_t* dst = a.acc + (size_t)m * a.N + n;
+          int32_t* o = a.acc + (size_t)m * a.N + n;
           if (vec) {
-            *reinterpret_cast<int4*>(dst) = make_int4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<int4*>(o) = make_int4(acc[0], acc[1], acc[2], acc[3]);
           } else {
-            for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = acc[e];
+            for (int e = 0; e < 4 && n + e < a.N; ++e) o[e] = acc[e];
           }
         } else {
-          uint16_t y[4];
+          const float sx_m = s_sx[c];
+          float y[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            y[e] = f32_to_bf16_rn(
-                __fadd_rn(__fmul_rn(__fmul_rn((float)acc[e], s_sx[col]), s_sw[rr + e]), s_bias[rr + e]));
-          uint16_t* dst = a.Y + (size_t)m * a.N + n;
+          for (int e = 0; e < 4; ++e) y[e] = fmaf((float)acc[e] * sx_m, s_sw[rr + e], s_bias[rr + e]);
+          uint16_t* o = a.Y + (size_t)m * a.N + n;
           if (vec) {
-            *reinterpret_cast<uint2*>(dst) = make_uint2((uint32_t)y[0] | ((uint32_t)y[1] << 16),
-                                                        (uint32_t)y[2] | ((uint32_t)y[3] << 16));
+            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2_rn(y[0], y[1]), pack_bf16x2_rn(y[2], y[3]));
           } else {
-            for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = y[e];
+            for (int e = 0; e < 4 && n + e < a.N; ++e) o[e] = f32_to_bf16_rn(y[e]);
           }
         }
       }
     }
-    cluster_sync_all();  // peers have finished reading this CTA's shared memory
+    __syncwarp();
+    cluster_wait();
   }
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
@@ -547,7 +637,7 @@ constexpr size_t kSmemPerSm = 233472;  // shared memory of one SM
 
 size_t stage_bytes(int bt) { return (size_t)bt * kBRow + (size_t)kTileN * kRawRow; }
 
-size_t smem_bytes(int bt, int stages) { return 1024 + stages * stage_bytes(bt) + (3 * stages + 6) * 8; }
+size_t smem_bytes(int bt, int stages) { return 1024 + stages * stage_bytes(bt) + (3 * stages + 7) * 8; }
 
 template <int BITS>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
@@ -596,9 +686,11 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     for (int s_try = s_want; s_try >= s_min; --s_try) {
       const int per_cta = (nkb + s_try - 1) / s_try;
       // stages: up to 6 within the shared-memory limit, no more than the
-      // k-blocks a CTA runs, and enough that the int32 partial tile of the
-      // split-K epilogue ([bt][128] int32) fits over them
-      const int ns_min = (int)(((size_t)bt * kTileN * 4 + stage_bytes(bt) - 1) / stage_bytes(bt));
+      // k-blocks a CTA runs, and enough that the 32-bit partial tile of the
+      // split-K epilogue (s_try slices of [bt][rows_per]) fits over them
+      const int rp = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+      const size_t part_bytes = (size_t)s_try * rp * bt * 4;
+      const int ns_min = (int)((part_bytes + stage_bytes(bt) - 1) / stage_bytes(bt));
       // tensor memory: accumulator [0, bt) (chunking: two float32 accumulators
       // and the int32 running sum), then one 32-column A slot per stage
       const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
@@ -620,7 +712,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       if (d < dyn_floor) d = dyn_floor;
       p.chunked = chunked; p.bt = bt; p.tiles_n = tiles_n; p.tiles_m = tiles_m;
       p.S = s_try; p.NS = ns; p.a_col = ac; p.cols = c; p.dyn = d;
-      p.rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+      p.rows_per = rp;
       found = true;
       const int active = vqlin::max_active_clusters((const void*)qgemm_kernel<BITS>, kThreads, d, s_try);
       p.one_wave = tiles_n * tiles_m <= active;

@@ -182,6 +182,36 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// Warp-collective forms: every lane of the warp executes the call (with
+// warp-uniform arguments) and one lane, chosen by elect.sync, issues the
+// instruction.  An MMA loop in which the whole warp runs the control flow
+// keeps the tensor core busy; the same loop run by one lane of a diverged
+// warp issues MMAs far more slowly.
+__device__ __forceinline__ void mma_f8f6f4_ta_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_ta_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -230,6 +260,20 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 
 // Waits until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Adds `bytes` (a multiple of 16) of 32-bit words from this CTA's shared
+// memory at `src` into the shared memory of a cluster peer at `dst`, on the
+// tensor-memory-access unit; completes `bytes` of transaction count on the
+// peer's mbarrier `mbar`.  `dst` and `mbar` are shared::cluster addresses
+// (mapa_shared); both addresses are 16-byte aligned.
+__device__ __forceinline__ void bulk_reduce_add_u32_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                            uint32_t mbar) {
+  asm volatile(
+      "cp.reduce.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes.add.u32 [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
 
 // Barrier among `count` threads (a multiple of 32) of the CTA on barrier `id`.
 __device__ __forceinline__ void named_barrier(int id, int count) {

@@ -189,35 +189,39 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop (every wait decided by a vote); one elected
+    // lane issues each MMA and commit
+    {
       const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
-      // stage, phase and group advance incrementally so the single issuing
-      // thread spends as few cycles as possible between MMAs
+      // stage, phase and group advance incrementally (no divisions)
       const uint64_t db0 = sdesc_sw128(base);
       const uint32_t ta0 = tmem + a.a_col;
       int s = 0, kin = 0, jl = 0;  // stage; k-block inside the group; local group
       uint32_t ph = 0;             // phase parity of stage s
       for (int i = 0; i < cnt; ++i) {
         const uint32_t acc = tmem + (uint32_t)((jl & 1) * BT);
-        if (kin == 0 && jl >= 2 &&
-            !mbar_wait_bounded(&acce[jl & 1], ((jl >> 1) - 1) & 1, a.wait_limit_ns, abort)) {
-          if (!*abort) record_timeout(a.status, abort);
-          break;
+        if (kin == 0 && jl >= 2) {
+          const bool ok = mbar_wait_bounded(&acce[jl & 1], ((jl >> 1) - 1) & 1, a.wait_limit_ns, abort);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (!ok && !*abort) record_timeout(a.status, abort);
+            break;
+          }
         }
-        if (!mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort)) {
-          if (!*abort) record_timeout(a.status, abort);
+        const bool ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (!ok && !*abort) record_timeout(a.status, abort);
           break;
         }
         tc_fence_after();
         const uint64_t db = db0 + (uint64_t)(s * (kStageBytes >> 4));
         const uint32_t ta = ta0 + (uint32_t)(s * kACols);
-        mma_f16_ta(acc, ta, db, id, kin != 0 ? 1u : 0u);
-        mma_f16_ta(acc, ta + 8, db + 2, id, 1u);
-        mma_f16_ta(acc, ta + 16, db + 4, id, 1u);
-        mma_f16_ta(acc, ta + 24, db + 6, id, 1u);
-        tc_commit(&empty[s]);
+        mma_f16_ta_warp(acc, ta, db, id, kin != 0 ? 1u : 0u);
+        mma_f16_ta_warp(acc, ta + 8, db + 2, id, 1u);
+        mma_f16_ta_warp(acc, ta + 16, db + 4, id, 1u);
+        mma_f16_ta_warp(acc, ta + 24, db + 6, id, 1u);
+        tc_commit_warp(&empty[s]);
         if (++kin == KB_PER_G) {
-          tc_commit(&accf[jl & 1]);
+          tc_commit_warp(&accf[jl & 1]);
           kin = 0;
           ++jl;
         }
@@ -226,7 +230,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           ph ^= 1u;
         }
       }
-      tc_commit(done);  // tensor memory is freed only after this completes
+      tc_commit_warp(done);  // tensor memory is freed only after this completes
     }
   } else if (warp < 10) {
     // ------------------------------------------------- weight expanders (2..9)
