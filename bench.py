@@ -55,7 +55,7 @@ def parse_args(argv=None):
                     help="prefix tokens per projection in the CPU-oracle sample")
     ap.add_argument("--shape", default=None,
                     help="time one kernel class alone instead of the control step: KIND,M,N,K with KIND in "
-                         "act_quant4, act_quant8, linear_w4a4, linear_w8a8, linear_w4a16, linear_bf16 "
+                         "act_quant4, act_quant8, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a16, linear_bf16 "
                          "(N is ignored for act_quant); prints a per-shape JSON line")
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -329,6 +329,9 @@ class ControlStepStack:
                 for gi, g in enumerate(self.exp_groups):
                     b, w, x = self.exp_buf[gi], self.exp_w[l][gi], self.exp_x[t][l][gi]
                     s = self.static[t, l, gi:gi + 1]
+                    # the activation kernel, then the GEMM: at 50 tokens this beats the GEMM that
+                    # quantizes on chip (linear_w4a4_static), whose every CTA re-quantizes its
+                    # activation tile
                     self._go(("act_quant_static", 4, self.M_exp, g["K"]),
                              lambda b=b, x=x, s=s: vq.act_hadamard_quant(x, 4, self.hb, static_scale=s,
                                                                          q_out=b["xq"], scale_out=b["sx"]))
@@ -366,6 +369,8 @@ class ControlStepStack:
         M, N, K = key[1], key[2], key[3]
         if kind == "linear_w4a4":
             return 2 * M * N * K, M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
+        if kind == "linear_w4a4_static":  # bf16 activations in, one scale
+            return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 + 4 * N + 2 * M * N
         if kind == "linear_w8a8":
             return 2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N
         if kind == "linear_w4a16":
@@ -619,7 +624,7 @@ def run_vqlin(args):
     if dom[0].startswith("act_quant") or dom[0] == "linear_w4a16" or dom[1] <= 64:
         bound, achieved, peak, unit = "hbm", nbytes / (dom_avg_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = f"hbm_gbs ({peaks_src})"
-    elif dom[0] == "linear_w4a4":
+    elif dom[0] in ("linear_w4a4", "linear_w4a4_static"):
         bound, unit = "tensor", "TFLOP/s"
         achieved = flops / (dom_avg_ms / 1e3) / 1e12
         peak = 2.0 * peaks["bf16_tflops"]
@@ -740,6 +745,14 @@ def run_shape(args):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
         run = lambda d: fn(xq, sx, d["wq"], d["sw"], out=y)  # noqa: E731
+    elif kind == "linear_w4a4_static":
+        per = N * K // 2
+        flops, nbytes = 2 * M * N * K, 2 * M * K + N * K // 2 + 4 + 4 * N + 2 * M * N
+        X = rand_bf16(M, K)
+        st = torch.full((1,), 0.5, device=dev)
+        mk = lambda: dict(wq=rand_codes(N, K, 4), sw=torch.rand(N, generator=g, device=dev))  # noqa: E731
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda d: vq.linear_w4a4_static(X, st, d["wq"], d["sw"], 128, out=y)  # noqa: E731
     elif kind == "linear_w4a16":
         per = N * K // 2
         flops, nbytes = 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // group + 2 * M * N

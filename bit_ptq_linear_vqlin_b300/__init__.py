@@ -27,7 +27,7 @@ from ._abi import LIB_PATH, VqlinError, check, load  # noqa: F401
 
 __all__ = [
     "VqlinError", "load", "LIB_PATH",
-    "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w8a8",
+    "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w4a4_static", "linear_w8a8",
     "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_withheld_loads",
     "get_last_device_error",
 ]
@@ -120,6 +120,30 @@ def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
         raise ValueError("wq must be [N, K/2] for xq [M, K]")
     return _linear_int(_lib.vqlin_linear_w4a4, "vqlin_linear_w4a4", xq, sx, wq, sw, bias, out,
                        xq.shape[1], stream)
+
+
+def linear_w4a4_static(X, static_scale, wq, sw, hadamard_block: int = 128, bias=None, out=None,
+                       stream=None):
+    """W4A4 with the activations quantized inside the GEMM at a static scale:
+    the same Y as act_hadamard_quant(X, 4, hadamard_block, static_scale) followed
+    by linear_w4a4.  X bf16 [M, K], static_scale float32 (one element), wq uint8
+    [N, K/2]."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(static_scale, "static_scale", torch.float32)
+    _need(wq, "wq", torch.uint8, 2)
+    _need(sw, "sw", torch.float32, 1)
+    M, K = X.shape
+    N = wq.shape[0]
+    if wq.shape[1] * 2 != K:
+        raise ValueError("wq must be [N, K/2] for X [M, K]")
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    check(_lib.vqlin_linear_w4a4_static(_ptr(X), _ptr(static_scale), hadamard_block, _ptr(wq), _ptr(sw),
+                                        _ptr(bias), _ptr(out), M, N, K, _stream(stream)),
+          "vqlin_linear_w4a4_static")
+    return out
 
 
 def linear_w8a8(xq, sx, wq, sw, bias=None, out=None, stream=None):

@@ -32,6 +32,7 @@ SIGNATURES = {
     "vqlin_quantize_weights_rtn": (_i, [_p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p]),
     "vqlin_act_hadamard_quant": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p]),
     "vqlin_linear_w4a4": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "vqlin_linear_w4a4_static": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w8a8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w4a16": (_i, [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_bf16_ref": (_i, [_p, _p, _p, _p, _i, _i, _i, _p]),

@@ -14,6 +14,7 @@
 //     butterflied in registers and only log2(LPG) stages use warp shuffles;
 //   * the per-token absmax is reduced over the token's threads (shuffles, then
 //     shared memory across warps); one CTA holds one or more whole tokens.
+#include "act_codes.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -28,39 +29,6 @@ struct BlockGeom {
   static constexpr int LPG = HB == 0 ? 1 : HB / 32;  // lanes per Hadamard block
   static constexpr int G = 32 * LPG;                   // channels per lane group
 };
-
-__device__ __forceinline__ void butterfly(float& a, float& b) {
-  float s = a + b, d = a - b;
-  a = s;
-  b = d;
-}
-
-// Codes of one 8-channel chunk in the integer GEMM's operand encoding:
-//   int4: one byte per code, s<<7 | |c| (the e4m3 bits of c * 2^-9) -> w[0..1];
-//   int8: one 16-bit word per code, s<<15 | |c| (the f16 bits of c * 2^-24)
-//         -> w[0..3].
-template <int BITS>
-__device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, float inv_s, uint32_t (&w)[4]) {
-  constexpr int qmax = (1 << (BITS - 1)) - 1;
-  w[0] = w[1] = w[2] = w[3] = 0;
-  if (s == 0.0f) return;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    // Fast quotient; near a rounding tie, redo with the IEEE division so the
-    // code equals rint(v / s) exactly (|t| <= 130 gives an error < 2^-10).
-    float t = v[e] * inv_s;
-    float rt = rintf(t);
-    if (fabsf(t - rt) > 0.4990234375f) rt = rintf(__fdiv_rn(v[e], s));
-    rt = fminf(fmaxf(rt, (float)(-qmax)), (float)qmax);
-    const uint32_t mag = (uint32_t)fabsf(rt);
-    const uint32_t neg = rt < 0.0f ? 1u : 0u;
-    if (BITS == 4) {
-      w[e >> 2] |= ((neg << 7) | mag) << (8 * (e & 3));
-    } else {
-      w[e >> 1] |= ((neg << 15) | mag) << (16 * (e & 1));
-    }
-  }
-}
 
 template <int BITS, int HB, int UPT>
 __global__ void __launch_bounds__(512)
@@ -99,42 +67,7 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
       v[i][j][4] = bf16_lo(raw.z); v[i][j][5] = bf16_hi(raw.z);
       v[i][j][6] = bf16_lo(raw.w); v[i][j][7] = bf16_hi(raw.w);
     }
-    if (HB > 0) {
-      // index bits 0..2: inside the chunk
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if ((e & h) == 0) butterfly(v[i][j][e], v[i][j][e + h]);
-      }
-      // the two index bits above the lane bits: which of the 4 chunks
-#pragma unroll
-      for (int h = 1; h < 4; h <<= 1)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((j & h) == 0)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) butterfly(v[i][j][e], v[i][j + h][e]);
-      // lane bits: partner lane holds the other half of each butterfly
-#pragma unroll
-      for (int mk = 1; mk < LPG; mk <<= 1) {
-        const float sg = (lane & mk) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float p = __shfl_xor_sync(0xffffffffu, v[i][j][e], mk);
-            v[i][j][e] = fmaf(v[i][j][e], sg, p);
-          }
-      }
-      const float c = HB == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(b)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[i][j][e] *= c;
-    }
+    if (HB > 0) hadamard_unit<HB == 0 ? 128 : HB>(v[i], lane);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll

@@ -54,6 +54,12 @@ cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
 vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq,
                              const float* sw, const uint16_t* bias, uint16_t* Y, int32_t* acc,
                              int M, int N, int K, int* status, cudaStream_t st);
+// W4A4 GEMM whose activations arrive as bf16 and are quantized on chip (block
+// Hadamard of hb = 64 or 128 channels, one static scale) instead of by a
+// separate activation kernel.
+vqlin_status launch_int_gemm_static_act(const uint16_t* X, const float* static_scale, int hb, const void* wq,
+                                       const float* sw, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                       int* status, cudaStream_t st);
 // The same GEMM with its producer withholding every tile load, so that the
 // consumers' bounded waits run out after limit_ns (failure-detection test).
 vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, int32_t* acc,

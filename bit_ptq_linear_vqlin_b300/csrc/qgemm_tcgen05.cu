@@ -45,6 +45,7 @@
 // VQLIN_ERR_TIMEOUT in the device status word and the CTA winds down.
 #include <mutex>
 
+#include "act_codes.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -57,7 +58,9 @@ constexpr int kRawRow = 64;       // packed weight bytes of one row per k-block
 constexpr int kBRow = 128;        // activation operand bytes of one row per k-block
 constexpr int kACols = 32;        // tensor-memory columns of one A stage (128 bytes per row)
 constexpr int kThreads = 320;     // 10 warps
+constexpr int kThreadsFx = 448;   // 14 warps: + 4 activation-quantizer warps (static-scale W4A4)
 constexpr int kExpandWarps = 8;
+constexpr int kQuantWarps = 4;
 constexpr int kMaxSplit = 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -81,6 +84,7 @@ struct QgemmArgs {
   int withhold_loads;    // test hook: the producer issues nothing (waits run out)
   int tma_store;         // unsplit K: stage the bf16 tile and store it with TMA
   int rows_per;          // split K: output channels each cluster rank owns
+  const float* static_scale;  // on-chip activation quantization: the static scale (one float)
 };
 
 // Expands 8 packed bytes into 4 words of A operand in channel order.
@@ -114,8 +118,10 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
   atomicCAS(status, 0, (int)VQLIN_ERR_TIMEOUT);
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads, 1)
+// FX: the activations arrive as bf16 and warps 10..13 quantize them on chip
+// (block Hadamard of HB channels, static scale) into the B operand.
+template <int BITS, bool FX, int HB>
+__global__ void __launch_bounds__(FX ? kThreadsFx : kThreads, 1)
 qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmY, const QgemmArgs a) {
   extern __shared__ uint8_t smem_dyn[];
@@ -127,13 +133,17 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int bt = a.bt;
   const uint32_t b_bytes = (uint32_t)bt * kBRow;                  // a multiple of 2048
-  const uint32_t stage_bytes = b_bytes + kTileN * kRawRow;        // [B operand | packed A]
+  const uint32_t xraw_off = b_bytes + kTileN * kRawRow;           // FX: bf16 activation tile
+  // [B operand | packed A | (FX) bf16 activations, two 64-channel halves]
+  const uint32_t stage_bytes = xraw_off + (FX ? (uint32_t)bt * 256u : 0u);
+  constexpr int NT = FX ? kThreadsFx : kThreads;
   const int NS = a.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * stage_bytes);
   uint64_t* full = bars;               // TMA -> expanders (both tiles landed)
   uint64_t* aready = bars + NS;        // expanders -> MMA (A stage in tensor memory)
   uint64_t* empty = bars + 2 * NS;     // MMA -> TMA (stage consumed)
-  uint64_t* acc_full = bars + 3 * NS;
+  uint64_t* bready = bars + 3 * NS;    // FX: quantizer -> MMA (B operand written)
+  uint64_t* acc_full = bars + 4 * NS;
   uint64_t* scl_ready = acc_full + 1;
   uint64_t* accf = acc_full + 2;       // [2] chunking: MMA -> drain (chunk accumulated)
   uint64_t* acce = acc_full + 4;       // [2] chunking: drain -> MMA (accumulator free)
@@ -154,6 +164,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       mbar_init(&full[i], 1);
       mbar_init(&aready[i], kExpandWarps / 2);  // one group of four warps per k-block
       mbar_init(&empty[i], 1);
+      mbar_init(&bready[i], kQuantWarps);
     }
     mbar_init(acc_full, 1);
     mbar_init(scl_ready, 31);
@@ -188,10 +199,11 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           bv[j] = in && a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n0 + i) << 16) : 0.0f;
         }
         pdl_wait();  // the per-token scales come from the previous kernel
+        const float xs = FX ? __ldg(a.static_scale) : 0.0f;  // one scale for every token
 #pragma unroll
         for (int j = 0; j < 9; ++j) {
           const int i = lane - 1 + 31 * j;
-          xv[j] = i < bt && m0 + i < a.M ? __ldg(a.sx + m0 + i) : 0.0f;
+          xv[j] = i < bt && m0 + i < a.M ? (FX ? xs : __ldg(a.sx + m0 + i)) : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < 5; ++j) {
@@ -218,18 +230,29 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       constexpr int kXStep = BITS == 4 ? kBRow : kBRow / 2;  // activation elements per k-block
+      // bytes one stage receives by TMA: packed weights and the activation
+      // tile (operand codes, or bf16 when quantized on chip)
+      const uint32_t tma_bytes = kTileN * kRawRow + (FX ? (uint32_t)bt * 256u : b_bytes);
+      auto load_x = [&](uint8_t* st, int kb, uint64_t* bar) {
+        if (FX) {
+          tma_load_2d(st + xraw_off, &tmX, kb * 128, m0, bar);
+          tma_load_2d(st + xraw_off + (uint32_t)bt * 128u, &tmX, kb * 128 + 64, m0, bar);
+        } else {
+          tma_load_2d(st, &tmX, kb * kXStep, m0, bar);
+        }
+      };
       int issued = 0;
       if (!a.withhold_loads) {
         // the weight tiles of the first stages do not depend on the previous
         // kernel: load them before waiting for it
         const int pre = cnt < NS ? cnt : NS;
         for (int i = 0; i < pre; ++i) {
-          mbar_arrive_expect_tx(&full[i], stage_bytes);
+          mbar_arrive_expect_tx(&full[i], tma_bytes);
           tma_load_2d(base + (size_t)i * stage_bytes + b_bytes, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
         }
         pdl_wait();
         for (int i = 0; i < pre; ++i) {
-          tma_load_2d(base + (size_t)i * stage_bytes, &tmX, (kb0 + i) * kXStep, m0, &full[i]);
+          load_x(base + (size_t)i * stage_bytes, kb0 + i, &full[i]);
           ++issued;
         }
         int s = 0;        // stage of k-block i
@@ -240,9 +263,9 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
             break;
           }
           uint8_t* st = base + (size_t)s * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          mbar_arrive_expect_tx(&full[s], tma_bytes);
           tma_load_2d(st + b_bytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
-          tma_load_2d(st, &tmX, (kb0 + i) * kXStep, m0, &full[s]);
+          load_x(st, kb0 + i, &full[s]);
           ++issued;
           if (++s == NS) {
             s = 0;
@@ -282,7 +305,8 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
             break;
           }
         }
-        const bool ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+        const bool ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort) &&
+                        (!FX || mbar_wait_bounded(&bready[s], ph, a.wait_limit_ns, abort));
         if (!__all_sync(0xffffffffu, ok)) {
           if (!ok && !*abort) record_timeout(a.status, abort);
           break;
@@ -316,7 +340,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       }
       tc_commit_warp(acc_full);
     }
-  } else {
+  } else if (warp < 2 + kExpandWarps) {
     // ------------------------------------------------- weight expanders (2..9)
     // thread = weight row (its warp's tensor-memory lane quadrant); the two
     // groups of four warps take alternate k-blocks, so one group's tensor
@@ -421,6 +445,61 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         if (!drain(drained++)) break;
     }
     (void)ok_all;
+  } else if (FX) {
+    // --------------------------------------- activation quantizers (10..13)
+    // The bf16 activation tile of each k-block (two 64-channel halves,
+    // 128-byte swizzle) becomes the B operand: block Hadamard over HB
+    // channels, then codes at the static scale, exactly as the standalone
+    // activation kernel computes them.  Four lanes hold one token's 128
+    // channels (32 each, the Hadamard unit layout); a warp takes 8 tokens per
+    // pass, the four warps 32.
+    constexpr int LPG = HB / 32;
+    const int qw = warp - (2 + kExpandWarps);
+    const int rl = lane >> 2, l4 = lane & 3;
+    const int g = l4 / LPG, l = l4 % LPG;  // Hadamard block inside the k-block; lane inside the block
+    pdl_wait();  // the static scale may come from the previous kernel
+    const float xs = __ldg(a.static_scale);
+    const float inv_s = xs > 0.0f ? __frcp_rn(xs) : 0.0f;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (!ok && !*abort) record_timeout(a.status, abort);
+        break;
+      }
+      const uint8_t* xr = base + (size_t)s * stage_bytes + xraw_off;
+      uint8_t* bq = base + (size_t)s * stage_bytes;
+      for (int r0 = qw * 8; r0 < bt; r0 += 8 * kQuantWarps) {  // warp-uniform
+        const int r = r0 + rl, sw7 = r & 7;
+        float v[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = HB * g + 8 * (l + LPG * j);  // first channel of chunk j
+          const uint4 raw = *reinterpret_cast<const uint4*>(xr + (size_t)(ch >> 6) * bt * 128 + r * 128 +
+                                                            ((((ch & 63) >> 3) ^ sw7) << 4));
+          v[j][0] = bf16_lo(raw.x); v[j][1] = bf16_hi(raw.x);
+          v[j][2] = bf16_lo(raw.y); v[j][3] = bf16_hi(raw.y);
+          v[j][4] = bf16_lo(raw.z); v[j][5] = bf16_hi(raw.z);
+          v[j][6] = bf16_lo(raw.w); v[j][7] = bf16_hi(raw.w);
+        }
+        hadamard_unit<HB>(v, lane);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w[4];
+          quantize_chunk<4>(v[j], xs, inv_s, w);
+          const int ch = HB * g + 8 * (l + LPG * j);
+          *reinterpret_cast<uint2*>(bq + r * 128 + ((((ch >> 4) ^ sw7)) << 4) + (ch & 8)) = make_uint2(w[0], w[1]);
+        }
+      }
+      fence_proxy_async_smem();  // the MMA reads these bytes through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bready[s]);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -428,8 +507,9 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   const bool chunked = BITS == 8 && a.chunk_kb > 0;
   const float unit = BITS == 4 ? 262144.0f : 281474976710656.0f;  // 2^18, 2^48: accumulator -> integer
   const bool raw_out = a.acc != nullptr;
+  const bool epi = warp >= 2 && warp < 2 + kExpandWarps;  // the epilogue's warps
   bool go = false;
-  if (warp >= 2) {
+  if (epi) {
     const bool ok = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, nullptr) &&
                     mbar_wait_bounded(scl_ready, 0, a.wait_limit_ns, nullptr);
     if (!ok) record_timeout(a.status, abort);
@@ -463,7 +543,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     // bf16 tile [bt tokens][128 channels] staged over the idle stages, then one
     // TMA store (the tensor map clips the M and N tails)
     uint16_t* ystage = reinterpret_cast<uint16_t*>(base);
-    if (warp >= 2) {
+    if (epi) {
       if (go) {
         const float sw_n = s_sw[row], b_n = s_bias[row];
         for (int cb = 16 * h; cb < bt; cb += 128) {
@@ -490,7 +570,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         }
         fence_proxy_async_smem();
       }
-      named_barrier(1, kThreads - 64);
+      named_barrier(1, kExpandWarps * 32);
       if (tid == 64 && go) {
         tma_store_2d(&tmY, n0, m0, ystage);
         bulk_commit();
@@ -502,7 +582,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   } else if (S == 1) {
     // straight from tensor memory to global memory: thread = channel, 16
     // tokens per load; for each token the warp writes 32 consecutive channels
-    if (warp >= 2 && go) {
+    if (epi && go) {
       const int n = n0 + row;
       const float sw_n = s_sw[row], b_n = s_bias[row];
       for (int cb = 16 * h; cb < bt; cb += 128) {
@@ -541,7 +621,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     const int own_n = own0 < kTileN ? min(rp, kTileN - own0) : 0;        // channels owned here
     uint32_t* part = reinterpret_cast<uint32_t*>(base);
     if (tid == 64 && own_n > 0) mbar_arrive_expect_tx(red_full, (uint32_t)(S - 1) * slice_bytes);
-    if (warp >= 2 && go) {
+    if (epi && go) {
       const int sl = row / rp, k = row - sl * rp;
       uint32_t* dst = part + (size_t)sl * slice_words + k;
       for (int cb = 16 * h; cb < bt; cb += 128) {
@@ -596,7 +676,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       const int total = nq * bt;
       const bool vec = (a.N & 3) == 0;
       const uint32_t* mine = part + (size_t)rank * slice_words;
-      for (int idx = tid; idx < total; idx += kThreads) {
+      for (int idx = tid; idx < total; idx += NT) {
         const int c = idx / nq, k = 4 * (idx - (idx / nq) * nq);
         const int m = m0 + c, rr = own0 + k, n = n0 + rr;
         if (m >= a.M || n >= a.N) continue;
@@ -635,20 +715,27 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
 constexpr int kMaxSmem = 232448 - 4096;
 constexpr size_t kSmemPerSm = 233472;  // shared memory of one SM
 
-size_t stage_bytes(int bt) { return (size_t)bt * kBRow + (size_t)kTileN * kRawRow; }
+// one pipeline stage: B operand, packed weights and (fx) the bf16 activation tile
+size_t stage_bytes(int bt, bool fx) {
+  return (size_t)bt * kBRow + (size_t)kTileN * kRawRow + (fx ? (size_t)bt * 256 : 0);
+}
 
-size_t smem_bytes(int bt, int stages) { return 1024 + stages * stage_bytes(bt) + (3 * stages + 7) * 8; }
+size_t smem_bytes(int bt, int stages, bool fx) { return 1024 + stages * stage_bytes(bt, fx) + (4 * stages + 7) * 8; }
 
-template <int BITS>
+// FX: bf16 activations quantized on chip at a static scale (xq is the bf16
+// activation matrix, sx the device pointer to the scale, HB the Hadamard block)
+template <int BITS, bool FX = false, int HB = 128>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
                          uint16_t* Y, int32_t* acc, int M, int N, int K, int* status, int withhold,
                          uint64_t limit_ns, cudaStream_t st) {
+  constexpr int NT = FX ? kThreadsFx : kThreads;
+  const auto kern = qgemm_kernel<BITS, FX, HB>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(qgemm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  std::call_once(attr_once, [kern] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(qgemm_kernel<BITS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr_err != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
@@ -690,7 +777,8 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       // split-K epilogue (s_try slices of [bt][rows_per]) fits over them
       const int rp = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
       const size_t part_bytes = (size_t)s_try * rp * bt * 4;
-      const int ns_min = (int)((part_bytes + stage_bytes(bt) - 1) / stage_bytes(bt));
+      const size_t sb = stage_bytes(bt, FX);
+      const int ns_min = (int)((part_bytes + sb - 1) / sb);
       // tensor memory: accumulator [0, bt) (chunking: two float32 accumulators
       // and the int32 running sum), then one 32-column A slot per stage
       const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
@@ -700,21 +788,21 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       if (ns > ns_tmem) ns = ns_tmem;
       if (ns < ns_min) ns = ns_min;
       if (ns < 2) ns = 2;
-      while (ns > ns_min && ns > 2 && smem_bytes(bt, ns) > (size_t)kMaxSmem) --ns;
+      while (ns > ns_min && ns > 2 && smem_bytes(bt, ns, FX) > (size_t)kMaxSmem) --ns;
       uint32_t c = 32;
       while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
-      if (c > 512 || smem_bytes(bt, ns) > (size_t)kMaxSmem) continue;
+      if (c > 512 || smem_bytes(bt, ns, FX) > (size_t)kMaxSmem) continue;
       // never more CTAs on an SM than its 512 tensor-memory columns hold: a
       // CTA blocked in tcgen05.alloc while its cluster peers wait for it could
       // otherwise wait on CTAs of another cluster in the same state
-      size_t d = smem_bytes(bt, ns);
+      size_t d = smem_bytes(bt, ns, FX);
       const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
       if (d < dyn_floor) d = dyn_floor;
       p.chunked = chunked; p.bt = bt; p.tiles_n = tiles_n; p.tiles_m = tiles_m;
       p.S = s_try; p.NS = ns; p.a_col = ac; p.cols = c; p.dyn = d;
       p.rows_per = rp;
       found = true;
-      const int active = vqlin::max_active_clusters((const void*)qgemm_kernel<BITS>, kThreads, d, s_try);
+      const int active = vqlin::max_active_clusters((const void*)kern, NT, d, s_try);
       p.one_wave = tiles_n * tiles_m <= active;
       if (p.one_wave) break;
     }
@@ -748,7 +836,10 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cuTensorMapEncodeTiled is unavailable");
   bool ok = vqlin::encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)w_row_bytes, (uint64_t)N,
                                   (uint64_t)w_row_bytes, kRawRow, kTileN, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (BITS == 4)
+  if (FX)
+    ok = ok && vqlin::encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xq, (uint64_t)K, (uint64_t)M,
+                                     (uint64_t)K * 2, 64, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B);
+  else if (BITS == 4)
     ok = ok && vqlin::encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M, (uint64_t)K,
                                      kBRow, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B);
   else
@@ -764,7 +855,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   }
 
   QgemmArgs a;
-  a.sx = sx; a.sw = sw; a.bias = bias; a.Y = Y; a.acc = acc; a.status = status;
+  a.sx = FX ? nullptr : sx; a.static_scale = FX ? sx : nullptr; a.sw = sw; a.bias = bias; a.Y = Y; a.acc = acc; a.status = status;
   a.M = M; a.N = N; a.K = K; a.bt = bt; a.nkb = nkb; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
   {
     const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
@@ -777,7 +868,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, S);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -789,7 +880,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, qgemm_kernel<BITS>, tmW, tmX, tmY, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, tmY, a);
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm launch (grid %d x %d x %d, cluster %d, %zu B smem): %s", tiles_n,
                        tiles_m, S, S, cfg.dynamicSmemBytes, cudaGetErrorString(e));
@@ -806,6 +897,15 @@ vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const vo
   if (M == 0 || N == 0) return VQLIN_OK;
   if (bits == 4) return launch_bits<4>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
   return launch_bits<8>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
+}
+
+vqlin_status launch_int_gemm_static_act(const uint16_t* X, const float* static_scale, int hb, const void* wq,
+                                       const float* sw, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                       int* status, cudaStream_t st) {
+  if (M == 0 || N == 0) return VQLIN_OK;
+  if (hb == 64)
+    return launch_bits<4, true, 64>(X, static_scale, wq, sw, bias, Y, nullptr, M, N, K, status, 0, kWaitLimitNs, st);
+  return launch_bits<4, true, 128>(X, static_scale, wq, sw, bias, Y, nullptr, M, N, K, status, 0, kWaitLimitNs, st);
 }
 
 vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, int32_t* acc, int M, int N, int K,

@@ -99,7 +99,7 @@ using vqlin::fail;
 
 extern "C" {
 
-int vqlin_version(void) { return 300; }
+int vqlin_version(void) { return 400; }
 
 const char* vqlin_status_string(vqlin_status s) {
   switch (s) {
@@ -219,6 +219,23 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
 vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                const uint16_t* bias, uint16_t* Y, int M, int N, int K, void* stream) {
   return linear_int(8, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
+}
+
+vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale, int hadamard_block,
+                                      const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
+                                      int N, int K, void* stream) {
+  REQUIRE(M >= 0 && N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
+  REQUIRE(hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
+          "hadamard_block must be 64 or 128 (got %d)", hadamard_block);
+  REQUIRE(K % 128 == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 128", K);
+  REQUIRE(K <= vqlin::kGemmW4MaxK, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K, vqlin::kGemmW4MaxK);
+  if (M == 0 || N == 0) return VQLIN_OK;
+  REQUIRE_PTR(X); REQUIRE_PTR(static_scale); REQUIRE_PTR(wq); REQUIRE_PTR(sw); REQUIRE_PTR(Y);
+  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(Y);
+  int* status = vqlin::device_status_word();
+  REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
+  return vqlin::launch_int_gemm_static_act(X, static_scale, hadamard_block, wq, sw, bias, Y, M, N, K, status,
+                                           static_cast<cudaStream_t>(stream));
 }
 
 vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int32_t* acc, int M, int N, int K,

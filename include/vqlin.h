@@ -142,6 +142,24 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
                                const float* sw, const uint16_t* bias, uint16_t* Y,
                                int M, int N, int K, void* stream);
 
+/*
+ * W4A4 projection with the activations quantized on chip at a static scale
+ * (Omega-QVLA "Scalatura delle Attivazioni DiT per Passo": per-step
+ * precomputed activation scales; FoldQuantVLA abstract: block Hadamard
+ * rotation and native integer execution).  Computes exactly what
+ * vqlin_act_hadamard_quant(X, M, K, 4, hadamard_block, static_scale, xq, sx)
+ * followed by vqlin_linear_w4a4(xq, sx, wq, sw, bias, Y, M, N, K) computes
+ * (the same codes bit for bit, hence the same Y) in one kernel, without the
+ * code matrix in memory.
+ * X: bf16 [M, K]; static_scale: ONE device float (> 0, finite); hadamard_block
+ * 64 or 128; wq, sw, bias, Y as for vqlin_linear_w4a4 (wq rotated with the same
+ * block).  Requires K % 128 == 0 and K <= 65536.
+ */
+vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale,
+                                      int hadamard_block, const uint8_t* wq, const float* sw,
+                                      const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                      void* stream);
+
 /* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
  * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands;
  * float32 partial sums cover at most 1024 channels, which bounds them below

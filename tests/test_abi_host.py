@@ -76,6 +76,12 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a4(A, None, A, A, None, A, 16, 16, 256, None) == INVALID
     assert lib.vqlin_linear_w4a4(A + 1, A, A, A, None, A, 16, 16, 256, None) == MISALIGNED
     assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 0, 16, 256, None) == OK
+    f = lib.vqlin_linear_w4a4_static
+    assert f(A, A, 128, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED    # K % 128
+    assert f(A, A, 32, A, A, None, A, 16, 16, 256, None) == INVALID         # block size
+    assert f(A, None, 128, A, A, None, A, 16, 16, 256, None) == INVALID     # null scale
+    assert f(A + 2, A, 128, A, A, None, A, 16, 16, 256, None) == MISALIGNED
+    assert f(A, A, 128, A, A, None, A, 0, 16, 256, None) == OK              # empty: no-op
     assert lib.vqlin_linear_w4a16(A, A, A, A, 96, None, A, 4, 16, 256, None) == INVALID
     assert lib.vqlin_linear_w4a16(A, A, A, A, 128, None, A, 4, 16, 192, None) == UNSUPPORTED
     assert lib.vqlin_linear_w4a16(A, A, A, None, 128, None, A, 4, 16, 256, None) == INVALID

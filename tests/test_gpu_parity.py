@@ -197,6 +197,57 @@ def test_weight_quant_zero_row():
     assert s.abs().max().item() == 0 and q.max().item() == 0
 
 
+STATIC_CASES = [
+    # (M, N, K, hb): the expert projections at 50 tokens, tails and both blocks
+    (50, 1024, 1024, 128), (50, 3072, 1024, 128), (50, 1024, 4096, 128), (50, 8192, 1024, 128),
+    (1, 128, 128, 128), (16, 256, 256, 64), (33, 300, 2048, 64), (130, 264, 1024, 128), (816, 256, 2048, 128),
+]
+
+
+@pytest.mark.parametrize("case", STATIC_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}b{c[3]}")
+def test_linear_w4a4_static_scale(case):
+    # activations quantized inside the GEMM at a static scale calibrated on
+    # another draw (so some codes clip)
+    M, N, K, hb = case
+    Xb = activations(M, K, n_outliers=max(1, K // 200), outlier_scale=20, seed=51)
+    Wb = weights(N, K, seed=52)
+    bias = weights(1, N, std=0.5, seed=53)[0]
+    s = o.calibrate_static_scale([activations(M, K, n_outliers=max(1, K // 200), outlier_scale=20, seed=54)], 4, hb)
+    ref = o.linear_quantized(Xb, Wb, 4, hb, bias_bits=bias, static_scale=s)
+    X, W, b = to_dev_bf16(Xb), to_dev_bf16(Wb), to_dev_bf16(bias)
+    wq, sw = vq.quantize_weights_rtn(W, 4, True, 0, hb)
+    st = torch.tensor([s], dtype=torch.float32, device=DEV)
+    yg = Guarded((M, N), torch.bfloat16)
+    vq.linear_w4a4_static(X, st, wq, sw, hb, b, out=yg.t)
+    yg.check()
+    vq.get_last_device_error()
+    y = bf16_bits(yg.t)
+    assert rel_fro(y, ref["y"]) <= 1e-3
+    # the same codes as the activation kernel, so the same output bit for bit
+    xq, sx = vq.act_hadamard_quant(X, 4, hb, static_scale=st)
+    check_act_codes(xq, sx, Xb, 4, hb, static_scale=s)
+    np.testing.assert_array_equal(y, bf16_bits(vq.linear_w4a4(xq, sx, wq, sw, b)))
+
+
+def test_linear_w4a4_static_scale_oracle_codes():
+    # with the oracle's codes (no rounding ties in this draw) the output is the
+    # oracle's within one bf16 ulp
+    M, N, K, hb = 50, 640, 1024, 128
+    Xb = activations(M, K, n_outliers=5, outlier_scale=20, seed=61)
+    Wb = weights(N, K, seed=62)
+    s = o.calibrate_static_scale([Xb], 4, hb)
+    ref = o.linear_quantized(Xb, Wb, 4, hb, static_scale=s)
+    X = to_dev_bf16(Xb)
+    st = torch.tensor([s], dtype=torch.float32, device=DEV)
+    xq, sx = vq.act_hadamard_quant(X, 4, hb, static_scale=st)
+    if not np.array_equal(decode_act(xq, 4), ref["xq"]):
+        pytest.skip("a rounding tie in this draw")
+    y = vq.linear_w4a4_static(X, st, torch.from_numpy(o.pack_int4(ref["wq"])).to(DEV),
+                              torch.from_numpy(ref["sw"]).to(DEV), hb)
+    ulp = np.abs(bf16_bits(y).astype(np.int64) - ref["y"].astype(np.int64))
+    assert ulp.max() <= 1 and (ulp > 0).mean() < 0.01
+
+
 @pytest.mark.parametrize("group", [64, 128, 256])
 @pytest.mark.parametrize("NK", [(1, 256), (7, 1024), (1024, 4096)])
 def test_weight_quant_asymmetric_bit_exact(group, NK):
