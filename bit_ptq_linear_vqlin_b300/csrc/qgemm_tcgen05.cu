@@ -767,10 +767,21 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
     s_want = s_want > nkb ? nkb : s_want;
     if (s_want < s_min) return false;
-    bool found = false;
-    // the largest split whose clusters are all resident at once (one wave);
-    // the smallest allowed one if none is
-    for (int s_try = s_want; s_try >= s_min; --s_try) {
+    // Among the splits whose clusters are all resident at once (one wave),
+    // the one of least estimated time: k-blocks per CTA x about 0.25 + 0.0004
+    // bt us each (on-chip activation quantization: about 1.5 us), plus about
+    // 1.2 + 0.008 bt + 0.17 S us for the split-K
+    // epilogue (measured on B300 for 16 <= bt <= 208; at 50 tokens and 8
+    // k-blocks no split is fastest).  With no one-wave split, the smallest.
+    auto est_us = [&](int s) {
+      // on-chip activation quantization costs far more per k-block than the MMAs
+      const double t_kb = FX ? 1.5 : 0.25 + 0.0004 * bt;
+      return ((nkb + s - 1) / s) * t_kb + (s > 1 ? 1.2 + 0.008 * bt + 0.17 * s : 0.0);
+    };
+    bool found = false, found_wave = false;
+    double best = 0.0;
+    for (int s_try = s_min; s_try <= s_want; ++s_try) {
+      Plan q;
       const int per_cta = (nkb + s_try - 1) / s_try;
       // stages: up to 6 within the shared-memory limit, no more than the
       // k-blocks a CTA runs, and enough that the 32-bit partial tile of the
@@ -798,13 +809,20 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       size_t d = smem_bytes(bt, ns, FX);
       const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
       if (d < dyn_floor) d = dyn_floor;
-      p.chunked = chunked; p.bt = bt; p.tiles_n = tiles_n; p.tiles_m = tiles_m;
-      p.S = s_try; p.NS = ns; p.a_col = ac; p.cols = c; p.dyn = d;
-      p.rows_per = rp;
-      found = true;
+      q.chunked = chunked; q.bt = bt; q.tiles_n = tiles_n; q.tiles_m = tiles_m;
+      q.S = s_try; q.NS = ns; q.a_col = ac; q.cols = c; q.dyn = d;
+      q.rows_per = rp;
       const int active = vqlin::max_active_clusters((const void*)kern, NT, d, s_try);
-      p.one_wave = tiles_n * tiles_m <= active;
-      if (p.one_wave) break;
+      q.one_wave = tiles_n * tiles_m <= active;
+      if (!found) {
+        p = q;  // the smallest allowed split
+        found = true;
+      }
+      if (q.one_wave && (!found_wave || est_us(s_try) < best)) {
+        p = q;
+        best = est_us(s_try);
+        found_wave = true;
+      }
     }
     return found;
   };
