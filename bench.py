@@ -55,7 +55,8 @@ def parse_args(argv=None):
                     help="prefix tokens per projection in the CPU-oracle sample")
     ap.add_argument("--shape", default=None,
                     help="time one kernel class alone instead of the control step: KIND,M,N,K with KIND in "
-                         "act_quant4, act_quant8, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a16, linear_bf16 "
+                         "act_quant4, act_quant8, act_quant_static4, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a16, "
+                         "linear_bf16 "
                          "(N is ignored for act_quant); prints a per-shape JSON line")
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -726,13 +727,15 @@ def run_shape(args):
 
     group = 128
     if kind.startswith("act_quant"):
+        # act_quant4 / act_quant8: dynamic per-token scales; act_quant_static4: one static scale
         bits = int(kind[-1])
         per = 2 * M * K
         flops, nbytes = 0, 2 * M * K + M * K * (1 if bits == 4 else 2) + 4 * M
         mk = lambda: dict(X=rand_bf16(M, K))  # noqa: E731
         q = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=dev)
         sx = torch.empty(M, device=dev)
-        run = lambda d: vq.act_hadamard_quant(d["X"], bits, 128, q_out=q, scale_out=sx)  # noqa: E731
+        st = torch.full((1,), 0.5, device=dev) if kind.startswith("act_quant_static") else None
+        run = lambda d: vq.act_hadamard_quant(d["X"], bits, 128, static_scale=st, q_out=q, scale_out=sx)  # noqa: E731
     elif kind in ("linear_w4a4", "linear_w8a8"):
         bits = 4 if kind == "linear_w4a4" else 8
         kb = K // 2 if bits == 4 else K           # packed weight bytes per row
