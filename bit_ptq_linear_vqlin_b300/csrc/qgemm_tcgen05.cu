@@ -26,21 +26,26 @@
 // Work decomposition (swap-AB: weights are the MMA's M side):
 //   * one CTA computes 128 output channels x BT tokens (BT <= 256, a multiple
 //     of 16) over a range of K; grid = (N/128, M/BT, S) with the S CTAs that
-//     share an output tile forming one thread-block cluster (split K);
+//     share an output tile forming one thread-block cluster (split K, S chosen
+//     per shape by an estimate of its time);
 //   * warp 0: TMA producer; a stage holds the activation operand tile and the
 //     packed weight tile (64 bytes of each of the 128 rows, 64-byte swizzle);
 //   * warps 2..9: expand the packed weights into the MMA's A operand directly
 //     in tensor memory (thread = weight row, tcgen05.st), so the expanded
 //     weights never pass through shared memory, whose bandwidth bounds the
-//     kernel otherwise;
-//   * warp 1: allocates tensor memory and issues the MMAs (one thread), 4 per
-//     k-block, A from tensor memory, B from shared memory, accumulating
-//     128 x BT float32 in tensor memory;
+//     kernel otherwise; the two groups of four warps take alternate k-blocks;
+//   * warp 1: allocates tensor memory and issues the MMAs, 4 per k-block, A
+//     from tensor memory, B from shared memory, accumulating 128 x BT float32
+//     in tensor memory; the whole warp runs the issue loop and one elected lane
+//     issues (a lone lane of a diverged warp issues too slowly);
 //   * epilogue (warps 2..9): unsplit K stages the bf16 tile in shared memory
-//     and writes it with one TMA store; split K converts to int32 in shared
-//     memory and, after a cluster barrier, each CTA sums its slice of the
-//     channels over the cluster's shared memory (DSMEM), so split K needs no
-//     global scratch memory and the sum is deterministic.
+//     and writes it with one TMA store; split K writes the partial tile as
+//     int32 slices over the idle stages and adds each slice into the cluster
+//     rank that owns those channels with one bulk reduction (reduce-scatter in
+//     shared memory), so split K needs no global scratch memory and its sum is
+//     exact;
+//   * variant FX (static-scale W4A4): the activations arrive as bf16 and warps
+//     10..13 rotate and quantize each k-block's tile on chip into the B operand.
 // Every wait is bounded in time; a wait that runs out records
 // VQLIN_ERR_TIMEOUT in the device status word and the CTA winds down.
 #include <mutex>
