@@ -128,7 +128,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&aready[i], kExpandWarps);
+      mbar_init(&aready[i], kExpandWarps / 2);  // one group of four warps per k-block
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -234,43 +234,58 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
   } else if (warp < 10) {
     // ------------------------------------------------- weight expanders (2..9)
-    // thread = weight row; the two warps of a lane quadrant take the two
-    // 16-byte halves of the row's 32 packed bytes (64 channels)
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    // thread = weight row; the two groups of four warps (one warp per lane
+    // quadrant each) take alternate k-blocks and expand the whole row (32
+    // packed bytes, 64 channels), so one group's tensor-memory stores are in
+    // flight while the other expands
+    const int q = warp & 3, gr = (warp - 2) >> 2;
     const int row = q * 32 + lane, n = n0 + row;
-    const int chunk = h ^ ((row >> 2) & 1);  // 32-byte swizzle of the packed tile
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col + (uint32_t)(16 * h);
-    uint32_t zz = ng > 0 ? zero_pair(a, n, g0) : 0u;
-    uint32_t zz_next = ng > 1 ? zero_pair(a, n, g0 + 1) : 0u;
-    int s = 0, kin = 0, jl = 0;  // stage; k-block inside the group; local group
-    uint32_t ph = 0;             // phase parity of stage s
-    for (int i = 0; i < cnt; ++i) {
+    const int sw = (row >> 2) & 1;  // 32-byte swizzle of the packed tile
+    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col;
+    // quantization group of this group's k-blocks: the next one differs by
+    // jstep (one group per k-block: 2, else 1)
+    constexpr int jstep = KB_PER_G == 1 ? 2 : 1;
+    int jl = gr / KB_PER_G, kin = gr % KB_PER_G;
+    uint32_t zz = jl < ng ? zero_pair(a, n, g0 + jl) : 0u;
+    uint32_t zz_next = jl + jstep < ng ? zero_pair(a, n, g0 + jl + jstep) : 0u;
+    int s = gr;        // stage of k-block i (NS >= 2)
+    uint32_t ph = 0;   // phase parity of stage s
+    for (int i = gr; i < cnt; i += 2) {
       const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
-      const uint4 c = *reinterpret_cast<const uint4*>(base + (size_t)s * kStageBytes + kBBytes + row * kRawRow +
-                                                      (chunk << 4));
-      uint32_t v[16];
-      dequant_word(c.x, zz, v);
-      dequant_word(c.y, zz, v + 4);
-      dequant_word(c.z, zz, v + 8);
-      dequant_word(c.w, zz, v + 12);
-      tmem_st_x16(trow + (uint32_t)(s * kACols), v);
+      const uint8_t* rawrow = base + (size_t)s * kStageBytes + kBBytes + row * kRawRow;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(rawrow + (sw << 4));
+      const uint4 c1 = *reinterpret_cast<const uint4*>(rawrow + ((1 ^ sw) << 4));
+      uint32_t v[2][16];
+      dequant_word(c0.x, zz, v[0]);
+      dequant_word(c0.y, zz, v[0] + 4);
+      dequant_word(c0.z, zz, v[0] + 8);
+      dequant_word(c0.w, zz, v[0] + 12);
+      dequant_word(c1.x, zz, v[1]);
+      dequant_word(c1.y, zz, v[1] + 4);
+      dequant_word(c1.z, zz, v[1] + 8);
+      dequant_word(c1.w, zz, v[1] + 12);
+      const uint32_t ta = trow + (uint32_t)(s * kACols);
+      tmem_st_x16(ta, v[0]);
+      tmem_st_x16(ta + 16, v[1]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aready[s]);
-      if (++s == NS) {
-        s = 0;
+      s += 2;
+      if (s >= NS) {
+        s -= NS;
         ph ^= 1u;
       }
-      if (++kin == KB_PER_G) {  // next group: rotate the zero points
-        kin = 0;
-        ++jl;
+      kin += 2;
+      if (kin >= KB_PER_G) {  // this group's next k-block is in another quantization group
+        kin -= KB_PER_G * (kin / KB_PER_G);
+        jl += jstep;
         zz = zz_next;
-        zz_next = jl + 1 < ng ? zero_pair(a, n, g0 + jl + 1) : 0u;
+        zz_next = jl + jstep < ng ? zero_pair(a, n, g0 + jl + jstep) : 0u;
       }
     }
   } else {
