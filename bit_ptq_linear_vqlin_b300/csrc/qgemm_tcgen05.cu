@@ -16,7 +16,7 @@
 //     c * 2^-24; the MMA is kind::f16 and the accumulator holds acc * 2^-48
 //     exactly while |acc| <= 127^2 * 1024 < 2^24, so the MMAs accumulate
 //     1024 channels at a time into one of two float32 buffers in tensor
-//     memory, and the expander warps add each finished chunk, converted to
+//     memory, and four drain warps add each finished chunk, converted to
 //     int32, into an int32 running sum there (exact for any K).
 // Activation codes arrive already in that operand encoding (one byte per int4
 // code, one 16-bit word per int8 code, written so by the activation kernel),
@@ -45,7 +45,9 @@
 //     shared memory), so split K needs no global scratch memory and its sum is
 //     exact;
 //   * variant FX (static-scale W4A4): the activations arrive as bf16 and warps
-//     10..13 rotate and quantize each k-block's tile on chip into the B operand.
+//     10..13 rotate and quantize each k-block's tile on chip into the B operand;
+//     int8: warps 10..13 add each finished 1024-channel chunk into the int32
+//     running sum (chunked plans) while the MMAs fill the other buffer.
 // Every wait is bounded in time; a wait that runs out records
 // VQLIN_ERR_TIMEOUT in the device status word and the CTA winds down.
 #include <mutex>
@@ -64,6 +66,7 @@ constexpr int kBRow = 128;        // activation operand bytes of one row per k-b
 constexpr int kACols = 32;        // tensor-memory columns of one A stage (128 bytes per row)
 constexpr int kThreads = 320;     // 10 warps
 constexpr int kThreadsFx = 448;   // 14 warps: + 4 activation-quantizer warps (static-scale W4A4)
+                                  // or 4 chunk-drain warps (int8)
 constexpr int kExpandWarps = 8;
 constexpr int kQuantWarps = 4;
 constexpr int kMaxSplit = 16;
@@ -126,7 +129,7 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
 // FX: the activations arrive as bf16 and warps 10..13 quantize them on chip
 // (block Hadamard of HB channels, static scale) into the B operand.
 template <int BITS, bool FX, int HB>
-__global__ void __launch_bounds__(FX ? kThreadsFx : kThreads, 1)
+__global__ void __launch_bounds__((FX || BITS == 8) ? kThreadsFx : kThreads, 1)
 qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmY, const QgemmArgs a) {
   extern __shared__ uint8_t smem_dyn[];
@@ -141,7 +144,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   const uint32_t xraw_off = b_bytes + kTileN * kRawRow;           // FX: bf16 activation tile
   // [B operand | packed A | (FX) bf16 activations, two 64-channel halves]
   const uint32_t stage_bytes = xraw_off + (FX ? (uint32_t)bt * 256u : 0u);
-  constexpr int NT = FX ? kThreadsFx : kThreads;
+  constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
   const int NS = a.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * stage_bytes);
   uint64_t* full = bars;               // TMA -> expanders (both tiles landed)
@@ -175,7 +178,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     mbar_init(scl_ready, 31);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], kExpandWarps);
+      mbar_init(&acce[i], 4);  // the four chunk-drain warps
     }
     mbar_init(red_full, 1);
     mbar_init_fence();
@@ -355,56 +358,12 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     const int sw = (row >> 1) & 3;  // 64-byte swizzle of the packed tile
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t trow = lanes + a.a_col;
-    const int ck = BITS == 8 ? a.chunk_kb : 0;  // int4 sums never need chunking
-    const float unit = 281474976710656.0f;  // 2^48: f16-operand accumulator -> integer
-    // chunking: adds float32 chunk c (exact integers x 2^-48, each below 2^24)
-    // into the int32 running sum; group g takes columns 16g, 16g + 32, ...
-    auto drain = [&](int c) -> bool {
-      const bool okc = mbar_wait_bounded(&accf[c & 1], (c >> 1) & 1, a.wait_limit_ns, abort);
-      if (!__all_sync(0xffffffffu, okc)) {
-        if (!okc && !*abort) record_timeout(a.status, abort);
-        return false;
-      }
-      tc_fence_after();
-      const uint32_t src = lanes + ((c & 1) ? a.d1_col : 0u);
-      for (int cb = 16 * g; cb < bt; cb += 64) {
-        const bool two = cb + 32 < bt;  // warp-uniform
-        uint32_t v[2][16], r[2][16];
-        tmem_ld_x16(src + (uint32_t)cb, v[0]);
-        if (two) tmem_ld_x16(src + (uint32_t)(cb + 32), v[1]);
-        if (c > 0) {
-          tmem_ld_x16(lanes + a.r_col + (uint32_t)cb, r[0]);
-          if (two) tmem_ld_x16(lanes + a.r_col + (uint32_t)(cb + 32), r[1]);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (u == 1 && !two) break;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            r[u][j] = (uint32_t)((c > 0 ? (int32_t)r[u][j] : 0) + __float2int_rn(__uint_as_float(v[u][j]) * unit));
-          tmem_st_x16(lanes + a.r_col + (uint32_t)(cb + 32 * u), r[u]);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[c & 1]);
-      return true;
-    };
-    bool ok_all = true;
-    int s = g, kin = g, c = 0, drained = 0;  // stage; k-block inside chunk c; chunks drained
-    uint32_t ph = 0;                          // phase parity of stage s
-    if (ck > 0)
-      while (kin >= ck) {
-        kin -= ck;
-        ++c;
-      }
+    int s = g;         // stage of k-block i (NS >= 2)
+    uint32_t ph = 0;   // phase parity of stage s
     for (int i = g; i < cnt; i += 2) {
       const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
-        ok_all = false;
         break;
       }
       const uint8_t* rawrow = base + (size_t)s * stage_bytes + b_bytes + row * kRawRow;
@@ -429,27 +388,48 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         s -= NS;
         ph ^= 1u;
       }
-      if (ck > 0) {
-        // chunks before the one of this k-block are complete: drain them
-        while (drained < c)
-          if (!drain(drained++)) {
-            ok_all = false;
-            break;
-          }
-        if (!ok_all) break;
-        kin += 2;
-        while (kin >= ck) {
-          kin -= ck;
-          ++c;
+    }
+  } else if (BITS == 8) {
+    // --------------------------------------------- int8 chunk drains (10..13)
+    // Chunking: adds float32 chunk c (exact integers x 2^-48, each below 2^24)
+    // into the int32 running sum in tensor memory, while the MMAs fill the
+    // other float32 buffer; warp = lane quadrant, all bt columns.
+    const int ck = a.chunk_kb;
+    const int nch = ck > 0 ? (cnt + ck - 1) / ck : 0;
+    const uint32_t lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float unit = 281474976710656.0f;  // 2^48: f16-operand accumulator -> integer
+    for (int c = 0; c < nch; ++c) {
+      const bool ok = mbar_wait_bounded(&accf[c & 1], (c >> 1) & 1, a.wait_limit_ns, abort);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (!ok && !*abort) record_timeout(a.status, abort);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t src = lanes + ((c & 1) ? a.d1_col : 0u);
+      for (int cb = 0; cb < bt; cb += 32) {
+        const bool two = cb + 16 < bt;  // warp-uniform
+        uint32_t v[2][16], r[2][16];
+        tmem_ld_x16(src + (uint32_t)cb, v[0]);
+        if (two) tmem_ld_x16(src + (uint32_t)(cb + 16), v[1]);
+        if (c > 0) {
+          tmem_ld_x16(lanes + a.r_col + (uint32_t)cb, r[0]);
+          if (two) tmem_ld_x16(lanes + a.r_col + (uint32_t)(cb + 16), r[1]);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (u == 1 && !two) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            r[u][j] = (uint32_t)((c > 0 ? (int32_t)r[u][j] : 0) + __float2int_rn(__uint_as_float(v[u][j]) * unit));
+          tmem_st_x16(lanes + a.r_col + (uint32_t)(cb + 16 * u), r[u]);
         }
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[c & 1]);
     }
-    if (ck > 0 && ok_all && cnt > 0) {
-      const int c_last = (cnt - 1) / (ck > 0 ? ck : 1);  // (a divisor the compiler sees as non-zero)
-      while (drained <= c_last)
-        if (!drain(drained++)) break;
-    }
-    (void)ok_all;
   } else if (FX) {
     // --------------------------------------- activation quantizers (10..13)
     // The bf16 activation tile of each k-block (two 64-channel halves,
@@ -515,8 +495,11 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   const bool epi = warp >= 2 && warp < 2 + kExpandWarps;  // the epilogue's warps
   bool go = false;
   if (epi) {
+    // chunked int8: the running sum is complete once the last chunk is drained
+    const int nch = chunked ? (cnt + a.chunk_kb - 1) / a.chunk_kb : 0;
     const bool ok = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, nullptr) &&
-                    mbar_wait_bounded(scl_ready, 0, a.wait_limit_ns, nullptr);
+                    mbar_wait_bounded(scl_ready, 0, a.wait_limit_ns, nullptr) &&
+                    (nch == 0 || mbar_wait_bounded(&acce[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.wait_limit_ns, nullptr));
     if (!ok) record_timeout(a.status, abort);
     tc_fence_after();
     // warp-uniform decision: the tensor-memory loads below are warp-collective
@@ -733,7 +716,7 @@ template <int BITS, bool FX = false, int HB = 128>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
                          uint16_t* Y, int32_t* acc, int M, int N, int K, int* status, int withhold,
                          uint64_t limit_ns, cudaStream_t st) {
-  constexpr int NT = FX ? kThreadsFx : kThreads;
+  constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
   const auto kern = qgemm_kernel<BITS, FX, HB>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
