@@ -144,45 +144,10 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_type, int m, int
          ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same MMAs with the A operand read from tensor memory (a_tmem: lane =
-// row of A, 32-bit column j = bytes 4j..4j+3 of the row along K).
-__device__ __forceinline__ void mma_f8f6f4_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Warp-collective forms: every lane of the warp executes the call (with
+// MMAs with the A operand read from tensor memory (a_tmem: lane = row of A,
+// 32-bit column j = bytes 4j..4j+3 of the row along K), B from shared memory
+// (descriptor b), D in tensor memory; accumulate = 0 overwrites D.
+// Warp-collective: every lane of the warp executes the call (with
 // warp-uniform arguments) and one lane, chosen by elect.sync, issues the
 // instruction.  An MMA loop in which the whole warp runs the control flow
 // keeps the tensor core busy; the same loop run by one lane of a diverged
@@ -205,6 +170,8 @@ __device__ __forceinline__ void mma_f16_ta_warp(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Arrives once on `bar` when every tcgen05 operation the issuing lane issued
+// before it has completed (warp-collective, as above).
 __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -212,13 +179,6 @@ __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
       : "memory");
 }
 
-// Arrives once on `bar` when every tcgen05 operation this thread issued
-// before it has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_addr(bar))
-               : "memory");
-}
 
 // 16 consecutive 32-bit columns of the warp's 32 lanes (lane quadrant =
 // warp index % 4); taddr carries the lane in bits 16..31.
@@ -306,14 +266,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 
 // 16-byte load from the shared memory of a cluster peer (address from mapa).
-__device__ __forceinline__ int4 ld_shared_cluster_v4(uint32_t addr) {
-  int4 v;
-  asm volatile("ld.shared::cluster.v4.s32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
 __device__ __forceinline__ float4 ld_shared_cluster_v4f(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
