@@ -71,6 +71,21 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def job_time_ms(ms_local: float, world: int, device) -> float:
+    """The job's timed region: the slowest rank's (all-reduce MAX over the process group)."""
+    if world == 1:
+        return ms_local
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, steps: int, ms_total: float) -> float:
+    """Whole-job throughput: every rank's steps over the slowest rank's time (weak scaling)."""
+    return world * steps / (ms_total / 1e3)
+
+
 # ----------------------------------------------------------------------------- peaks
 
 def load_peaks():
@@ -525,13 +540,9 @@ def run_vqlin(args):
     if world > 1:
         torch.distributed.barrier()
     clock_info = clocks.stop()
-    ms_total = ev[0].elapsed_time(ev[1])
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = job_time_ms(ev[0].elapsed_time(ev[1]), world, dev)
     ms_step = ms_total / args.steps
-    value = world * args.steps / (ms_total / 1e3)
+    value = job_value(world, args.steps, ms_total)
 
     # -- per kernel class: every launch of the class in one step (all layers,
     # so the weights rotate exactly as in the step), captured back to back in
