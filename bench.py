@@ -27,6 +27,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -417,7 +418,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples (the JSON line carries their summary); VQLIN_CLOCKS_DIR keeps them
+        out_dir = os.environ.get("VQLIN_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"vqlin_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
