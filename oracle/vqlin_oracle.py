@@ -383,14 +383,16 @@ def linear_epilogue(acc, sx, sw, bias_bits=None) -> np.ndarray:
 
 
 def linear_quantized(X_bits, W_bits, bits: int, hadamard_block: int,
-                     bias_bits=None, static_scale=None):
-    """Whole W4A4 / W8A8 projection from bf16 inputs to bf16 output.
+                     bias_bits=None, static_scale=None, act_bits=None):
+    """Whole W4A4 / W8A8 projection from bf16 inputs to bf16 output; with
+    act_bits = 8 and bits = 4, the W4A8 projection (int4 weights, int8
+    per-token activations: the QuantVLA setting, "W4A8" in its results).
 
     Returns dict with the activation codes/scales, weight codes/scales, the
     int64 accumulators and the bf16 output bits.
     """
     wt = quantize_weights_rtn(W_bits, bits, True, 0, hadamard_block)
-    xq, sx = act_hadamard_quant(X_bits, bits, hadamard_block, static_scale)
+    xq, sx = act_hadamard_quant(X_bits, bits if act_bits is None else act_bits, hadamard_block, static_scale)
     acc = int_gemm(xq, wt["q"])
     y = linear_epilogue(acc, sx, wt["s"], bias_bits)
     return dict(xq=xq, sx=sx, wq=wt["q"], sw=wt["s"], acc=acc, y=y)

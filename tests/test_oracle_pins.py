@@ -329,13 +329,14 @@ def test_linear_bf16_bruteforce():
 
 # ---------------------------------------------------------------- whole projection
 
-@pytest.mark.parametrize("bits,b", [(4, 64), (4, 128), (8, 128), (4, 0)])
-def test_quantized_linear_within_rtn_error_bound(bits, b):
+@pytest.mark.parametrize("bits,b,abits", [(4, 64, 4), (4, 128, 4), (8, 128, 8), (4, 0, 4), (4, 128, 8)])
+def test_quantized_linear_within_rtn_error_bound(bits, b, abits):
     """|y - x.W^T| <= sum_k (|x~| s_w/2 + |w~| s_x/2 + s_x s_w/4) + half a bf16 ulp."""
     M, N, K = 8, 16, 256
     xb = activations(M, K, n_outliers=4, outlier_scale=20, seed=21)
     wb = weights(N, K, seed=22)
-    r = o.linear_quantized(xb, wb, bits, b)
+    r = o.linear_quantized(xb, wb, bits, b, act_bits=abits)
+    assert np.abs(r["xq"]).max() <= (7 if abits == 4 else 127) and np.abs(r["wq"]).max() <= (7 if bits == 4 else 127)
     x, w = o.bf16_to_f64(xb), o.bf16_to_f64(wb)
     exact = x @ w.T
     xt = np.abs(o.block_hadamard_rotate(x, b))
@@ -358,6 +359,22 @@ def test_rotation_reduces_w4a4_error_on_outlier_inputs():
     e_plain = np.linalg.norm(o.bf16_to_f64(o.linear_quantized(xb, wb, 4, 0)["y"]) - exact)
     e_rot = np.linalg.norm(o.bf16_to_f64(o.linear_quantized(xb, wb, 4, 128)["y"]) - exact)
     assert e_rot < 0.5 * e_plain
+
+
+def test_w4a8_sits_between_w4a4_and_w8a8():
+    # 8-bit activations remove the activation part of the W4A4 error; 4-bit
+    # weights keep the weight part that W8A8 does not have
+    M, N, K = 32, 64, 512
+    xb = activations(M, K, n_outliers=5, outlier_scale=20, seed=33)
+    wb = weights(N, K, seed=34)
+    exact = o.bf16_to_f64(xb) @ o.bf16_to_f64(wb).T
+    err = {name: np.linalg.norm(o.bf16_to_f64(o.linear_quantized(xb, wb, wbits, 128, act_bits=abits)["y"]) - exact)
+           for name, wbits, abits in (("w4a4", 4, 4), ("w4a8", 4, 8), ("w8a8", 8, 8))}
+    assert err["w8a8"] < err["w4a8"] < err["w4a4"]
+    # same weight codes as W4A4 and same activation codes as W8A8
+    r48 = o.linear_quantized(xb, wb, 4, 128, act_bits=8)
+    assert np.array_equal(r48["wq"], o.linear_quantized(xb, wb, 4, 128)["wq"])
+    assert np.array_equal(r48["xq"], o.linear_quantized(xb, wb, 8, 128)["xq"])
 
 
 def test_static_scale_calibration_is_max_of_dynamic_scales():
