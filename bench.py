@@ -56,7 +56,8 @@ def parse_args(argv=None):
                     help="prefix tokens per projection in the CPU-oracle sample")
     ap.add_argument("--shape", default=None,
                     help="time one kernel class alone instead of the control step: KIND,M,N,K with KIND in "
-                         "act_quant4, act_quant8, act_quant_static4, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a16, "
+                         "act_quant4, act_quant8, act_quant_static4, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a8, "
+                         "linear_w4a16, "
                          "linear_bf16 "
                          "(N is ignored for act_quant); prints a per-shape JSON line")
     a = ap.parse_args(argv)
@@ -390,6 +391,8 @@ class ControlStepStack:
             return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 + 4 * N + 2 * M * N
         if kind == "linear_w8a8":
             return 2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N
+        if kind == "linear_w4a8":
+            return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
         if kind == "linear_w4a16":
             return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // self.group + 2 * M * N
         raise KeyError(key)
@@ -750,17 +753,18 @@ def run_shape(args):
         sx = torch.empty(M, device=dev)
         st = torch.full((1,), 0.5, device=dev) if kind.startswith("act_quant_static") else None
         run = lambda d: vq.act_hadamard_quant(d["X"], bits, 128, static_scale=st, q_out=q, scale_out=sx)  # noqa: E731
-    elif kind in ("linear_w4a4", "linear_w8a8"):
-        bits = 4 if kind == "linear_w4a4" else 8
-        kb = K // 2 if bits == 4 else K           # packed weight bytes per row
+    elif kind in ("linear_w4a4", "linear_w8a8", "linear_w4a8"):
+        bits = 4 if kind == "linear_w4a4" else 8  # activation bits
+        wbits = 8 if kind == "linear_w8a8" else 4
+        kb = K // 2 if wbits == 4 else K          # packed weight bytes per row
         xb = K if bits == 4 else 2 * K            # activation operand bytes per token
         per = N * kb
         flops, nbytes = 2 * M * N * K, M * xb + N * kb + 4 * M + 4 * N + 2 * M * N
         xq = rand_act_codes(M, K, bits)
         sx = torch.rand(M, generator=g, device=dev)
-        mk = lambda: dict(wq=rand_codes(N, K, bits), sw=torch.rand(N, generator=g, device=dev))  # noqa: E731
+        mk = lambda: dict(wq=rand_codes(N, K, wbits), sw=torch.rand(N, generator=g, device=dev))  # noqa: E731
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
+        fn = {"linear_w4a4": vq.linear_w4a4, "linear_w8a8": vq.linear_w8a8, "linear_w4a8": vq.linear_w4a8}[kind]
         run = lambda d: fn(xq, sx, d["wq"], d["sw"], out=y)  # noqa: E731
     elif kind == "linear_w4a4_static":
         per = N * K // 2

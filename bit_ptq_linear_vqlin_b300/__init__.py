@@ -28,7 +28,8 @@ from ._abi import LIB_PATH, VqlinError, check, load  # noqa: F401
 __all__ = [
     "VqlinError", "load", "LIB_PATH",
     "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w4a4_static", "linear_w8a8",
-    "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_withheld_loads",
+    "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
+    "debug_gemm_withheld_loads",
     "get_last_device_error",
 ]
 
@@ -156,6 +157,17 @@ def linear_w8a8(xq, sx, wq, sw, bias=None, out=None, stream=None):
                        xq.shape[1], stream)
 
 
+def linear_w4a8(xq, sx, wq, sw, bias=None, out=None, stream=None):
+    """Y = bf16(int_gemm(xq, wq) * sx * sw + bias): xq int16 [M, K] (int8 activation
+    codes), wq uint8 [N, K/2] (int4 weight codes)."""
+    _need(xq, "xq", torch.int16, 2)
+    _need(wq, "wq", torch.uint8, 2)
+    if wq.shape[1] * 2 != xq.shape[1]:
+        raise ValueError("wq must be [N, K/2] for xq [M, K]")
+    return _linear_int(_lib.vqlin_linear_w4a8, "vqlin_linear_w4a8", xq, sx, wq, sw, bias, out,
+                       xq.shape[1], stream)
+
+
 def linear_w4a16(X, wq, scales, zeros, group_size: int = 128, bias=None, out=None, stream=None):
     """Y = bf16(X . dequant(wq, scales, zeros)^T + bias), weight-only int4."""
     _need(X, "X", torch.bfloat16, 2)
@@ -196,6 +208,16 @@ def debug_gemm_s32(bits: int, xq, wq, K: int, out=None, stream=None):
         out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
     check(_lib.vqlin_debug_gemm_s32(bits, _ptr(xq), _ptr(wq), _ptr(out), M, N, K, _stream(stream)),
           "vqlin_debug_gemm_s32")
+    return out
+
+
+def debug_gemm_w4a8_s32(xq, wq, K: int, out=None, stream=None):
+    """int32 accumulators of the W4A8 integer GEMM (xq int16 [M, K], wq uint8 [N, K/2])."""
+    M, N = xq.shape[0], wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    check(_lib.vqlin_debug_gemm_w4a8_s32(_ptr(xq), _ptr(wq), _ptr(out), M, N, K, _stream(stream)),
+          "vqlin_debug_gemm_w4a8_s32")
     return out
 
 

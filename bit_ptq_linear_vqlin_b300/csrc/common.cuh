@@ -54,6 +54,11 @@ cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
 vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const void* wq,
                              const float* sw, const uint16_t* bias, uint16_t* Y, int32_t* acc,
                              int M, int N, int K, int* status, cudaStream_t st);
+// W4A8 GEMM: int4 weight codes [N, K/2] (as for W4A4) against int8 activation
+// codes [M, K] (16-bit operand words); acc == nullptr as above.
+vqlin_status launch_int_gemm_w4a8(const void* xq, const float* sx, const void* wq, const float* sw,
+                                  const uint16_t* bias, uint16_t* Y, int32_t* acc, int M, int N, int K, int* status,
+                                  cudaStream_t st);
 // W4A4 GEMM whose activations arrive as bf16 and are quantized on chip (block
 // Hadamard of hb = 64 or 128 channels, one static scale) instead of by a
 // separate activation kernel.

@@ -44,6 +44,9 @@
 //     rank that owns those channels with one bulk reduction (reduce-scatter in
 //     shared memory), so split K needs no global scratch memory and its sum is
 //     exact;
+//   * variant W4 (W4A8): int4 weights (nibbles, 32 bytes per row and 64-channel
+//     k-block) expanded to f16 operands against int8 activations; the sums
+//     stay exact over 16384 channels (7 x 127 per product);
 //   * variant FX (static-scale W4A4): the activations arrive as bf16 and warps
 //     10..13 rotate and quantize each k-block's tile on chip into the B operand;
 //     int8: warps 10..13 add each finished 1024-channel chunk into the int32
@@ -121,6 +124,18 @@ __device__ __forceinline__ void expand8(uint32_t lo, uint32_t hi, uint32_t* o) {
   }
 }
 
+// W4A8: one word of 8 packed int4 codes (nibble s|mmm, even channel in the low
+// nibble of each byte) -> 4 words of f16 operand pairs s<<15 | mmm (the f16
+// bits of c * 2^-24), channel order.
+__device__ __forceinline__ void expand_nib_f16(uint32_t w, uint32_t* o) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b = (w >> (8 * i)) & 0xFFu;
+    const uint32_t t = (b & 0x0Fu) | ((b & 0xF0u) << 12);  // even channel bits 0..3, odd 16..19
+    o[i] = (t & 0x00070007u) | ((t & 0x00080008u) << 12);
+  }
+}
+
 __device__ __forceinline__ void record_timeout(int* status, volatile int* abort) {
   *abort = 1;
   atomicCAS(status, 0, (int)VQLIN_ERR_TIMEOUT);
@@ -128,7 +143,9 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
 
 // FX: the activations arrive as bf16 and warps 10..13 quantize them on chip
 // (block Hadamard of HB channels, static scale) into the B operand.
-template <int BITS, bool FX, int HB>
+// W4 (with BITS = 8): W4A8, int4 weights (packed nibbles, 32 bytes per row and
+// k-block) against int8 activations, on the f16 MMAs.
+template <int BITS, bool FX, int HB, bool W4>
 __global__ void __launch_bounds__((FX || BITS == 8) ? kThreadsFx : kThreads, 1)
 qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmY, const QgemmArgs a) {
@@ -141,7 +158,8 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int bt = a.bt;
   const uint32_t b_bytes = (uint32_t)bt * kBRow;                  // a multiple of 2048
-  const uint32_t xraw_off = b_bytes + kTileN * kRawRow;           // FX: bf16 activation tile
+  constexpr int RAW = (BITS == 8 && W4) ? 32 : kRawRow;           // packed weight bytes per row and k-block
+  const uint32_t xraw_off = b_bytes + kTileN * RAW;               // FX: bf16 activation tile
   // [B operand | packed A | (FX) bf16 activations, two 64-channel halves]
   const uint32_t stage_bytes = xraw_off + (FX ? (uint32_t)bt * 256u : 0u);
   constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
@@ -240,7 +258,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
       constexpr int kXStep = BITS == 4 ? kBRow : kBRow / 2;  // activation elements per k-block
       // bytes one stage receives by TMA: packed weights and the activation
       // tile (operand codes, or bf16 when quantized on chip)
-      const uint32_t tma_bytes = kTileN * kRawRow + (FX ? (uint32_t)bt * 256u : b_bytes);
+      const uint32_t tma_bytes = kTileN * RAW + (FX ? (uint32_t)bt * 256u : b_bytes);
       auto load_x = [&](uint8_t* st, int kb, uint64_t* bar) {
         if (FX) {
           tma_load_2d(st + xraw_off, &tmX, kb * 128, m0, bar);
@@ -256,7 +274,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         const int pre = cnt < NS ? cnt : NS;
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx(&full[i], tma_bytes);
-          tma_load_2d(base + (size_t)i * stage_bytes + b_bytes, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
+          tma_load_2d(base + (size_t)i * stage_bytes + b_bytes, &tmW, (kb0 + i) * RAW, n0, &full[i]);
         }
         pdl_wait();
         for (int i = 0; i < pre; ++i) {
@@ -272,7 +290,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           }
           uint8_t* st = base + (size_t)s * stage_bytes;
           mbar_arrive_expect_tx(&full[s], tma_bytes);
-          tma_load_2d(st + b_bytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
+          tma_load_2d(st + b_bytes, &tmW, (kb0 + i) * RAW, n0, &full[s]);
           load_x(st, kb0 + i, &full[s]);
           ++issued;
           if (++s == NS) {
@@ -355,7 +373,9 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     // memory stores are in flight while the other group expands
     const int q = warp & 3, g = (warp - 2) >> 2;
     const int row = q * 32 + lane;
-    const int sw = (row >> 1) & 3;  // 64-byte swizzle of the packed tile
+    // swizzle of the packed tile: 64-byte rows (int4 / int8 weights), or 32-byte
+    // rows (W4A8: 64 channels of nibbles)
+    const int sw = RAW == 64 ? (row >> 1) & 3 : (row >> 2) & 1;
     const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t trow = lanes + a.a_col;
     int s = g;         // stage of k-block i (NS >= 2)
@@ -366,15 +386,27 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
-      const uint8_t* rawrow = base + (size_t)s * stage_bytes + b_bytes + row * kRawRow;
-      uint4 rw[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) rw[j] = *reinterpret_cast<const uint4*>(rawrow + ((j ^ sw) << 4));
+      const uint8_t* rawrow = base + (size_t)s * stage_bytes + b_bytes + row * RAW;
       uint32_t v[2][16];
+      if (RAW == 32) {
+        // W4A8: 16 bytes = 32 channels -> 16 f16 pair words per half
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        expand8<BITS>(rw[j].x, rw[j].y, &v[j >> 1][8 * (j & 1)]);
-        expand8<BITS>(rw[j].z, rw[j].w, &v[j >> 1][8 * (j & 1) + 4]);
+        for (int j = 0; j < 2; ++j) {
+          const uint4 r = *reinterpret_cast<const uint4*>(rawrow + ((j ^ sw) << 4));
+          expand_nib_f16(r.x, &v[j][0]);
+          expand_nib_f16(r.y, &v[j][4]);
+          expand_nib_f16(r.z, &v[j][8]);
+          expand_nib_f16(r.w, &v[j][12]);
+        }
+      } else {
+        uint4 rw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rw[j] = *reinterpret_cast<const uint4*>(rawrow + ((j ^ sw) << 4));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          expand8<BITS>(rw[j].x, rw[j].y, &v[j >> 1][8 * (j & 1)]);
+          expand8<BITS>(rw[j].z, rw[j].w, &v[j >> 1][8 * (j & 1) + 4]);
+        }
       }
       const uint32_t ta = trow + (uint32_t)(s * kACols);
       tmem_st_x16(ta, v[0]);
@@ -703,21 +735,25 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
 constexpr int kMaxSmem = 232448 - 4096;
 constexpr size_t kSmemPerSm = 233472;  // shared memory of one SM
 
-// one pipeline stage: B operand, packed weights and (fx) the bf16 activation tile
-size_t stage_bytes(int bt, bool fx) {
-  return (size_t)bt * kBRow + (size_t)kTileN * kRawRow + (fx ? (size_t)bt * 256 : 0);
+// one pipeline stage: B operand, packed weights (raw bytes per row) and (fx)
+// the bf16 activation tile
+size_t stage_bytes(int bt, bool fx, int raw) {
+  return (size_t)bt * kBRow + (size_t)kTileN * raw + (fx ? (size_t)bt * 256 : 0);
 }
 
-size_t smem_bytes(int bt, int stages, bool fx) { return 1024 + stages * stage_bytes(bt, fx) + (4 * stages + 7) * 8; }
+size_t smem_bytes(int bt, int stages, bool fx, int raw) {
+  return 1024 + stages * stage_bytes(bt, fx, raw) + (4 * stages + 7) * 8;
+}
 
 // FX: bf16 activations quantized on chip at a static scale (xq is the bf16
 // activation matrix, sx the device pointer to the scale, HB the Hadamard block)
-template <int BITS, bool FX = false, int HB = 128>
+template <int BITS, bool FX = false, int HB = 128, bool W4 = false>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
                          uint16_t* Y, int32_t* acc, int M, int N, int K, int* status, int withhold,
                          uint64_t limit_ns, cudaStream_t st) {
   constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
-  const auto kern = qgemm_kernel<BITS, FX, HB>;
+  const auto kern = qgemm_kernel<BITS, FX, HB, W4>;
+  constexpr int RAW = (BITS == 8 && W4) ? 32 : kRawRow;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [kern] {
@@ -729,7 +765,10 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
 
   const int kb_codes = BITS == 4 ? 128 : 64;
-  const int w_row_bytes = BITS == 4 ? K / 2 : K;
+  const int w_row_bytes = (BITS == 4 || W4) ? K / 2 : K;
+  // f16-operand sums are exact while below 2^24: 1024 channels of int8 x int8
+  // (127^2 per product), 16384 of int4 x int8 (7 x 127)
+  const int exact_ch = W4 ? 16384 : 1024;
   const int nkb = K / kb_codes;
 
   // One launch plan: token tile, K split, stages, tensor-memory columns and
@@ -776,7 +815,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       // split-K epilogue (s_try slices of [bt][rows_per]) fits over them
       const int rp = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
       const size_t part_bytes = (size_t)s_try * rp * bt * 4;
-      const size_t sb = stage_bytes(bt, FX);
+      const size_t sb = stage_bytes(bt, FX, RAW);
       const int ns_min = (int)((part_bytes + sb - 1) / sb);
       // tensor memory: accumulator [0, bt) (chunking: two float32 accumulators
       // and the int32 running sum), then one 32-column A slot per stage
@@ -787,14 +826,14 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       if (ns > ns_tmem) ns = ns_tmem;
       if (ns < ns_min) ns = ns_min;
       if (ns < 2) ns = 2;
-      while (ns > ns_min && ns > 2 && smem_bytes(bt, ns, FX) > (size_t)kMaxSmem) --ns;
+      while (ns > ns_min && ns > 2 && smem_bytes(bt, ns, FX, RAW) > (size_t)kMaxSmem) --ns;
       uint32_t c = 32;
       while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
-      if (c > 512 || smem_bytes(bt, ns, FX) > (size_t)kMaxSmem) continue;
+      if (c > 512 || smem_bytes(bt, ns, FX, RAW) > (size_t)kMaxSmem) continue;
       // never more CTAs on an SM than its 512 tensor-memory columns hold: a
       // CTA blocked in tcgen05.alloc while its cluster peers wait for it could
       // otherwise wait on CTAs of another cluster in the same state
-      size_t d = smem_bytes(bt, ns, FX);
+      size_t d = smem_bytes(bt, ns, FX, RAW);
       const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
       if (d < dyn_floor) d = dyn_floor;
       q.chunked = chunked; q.bt = bt; q.tiles_n = tiles_n; q.tiles_m = tiles_m;
@@ -816,11 +855,11 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   };
   Plan plan;
   bool have = false;
-  if (BITS == 8 && K > 1024) {
-    // int8: split K over a cluster so no CTA sums more than 1024 channels if
-    // that runs in one wave, else chunk inside each CTA
+  if (BITS == 8 && K > exact_ch) {
+    // int8 activations: split K over a cluster so no CTA sums more than
+    // exact_ch channels if that runs in one wave, else chunk inside each CTA
     Plan split;
-    if (make_plan(false, (K + 1023) / 1024, split) && split.one_wave) {
+    if (make_plan(false, (K + exact_ch - 1) / exact_ch, split) && split.one_wave) {
       plan = split;
       have = true;
     } else {
@@ -841,7 +880,8 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   if (!vqlin::tmap_encoder_available())
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cuTensorMapEncodeTiled is unavailable");
   bool ok = vqlin::encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)w_row_bytes, (uint64_t)N,
-                                  (uint64_t)w_row_bytes, kRawRow, kTileN, CU_TENSOR_MAP_SWIZZLE_64B);
+                                  (uint64_t)w_row_bytes, RAW, kTileN,
+                                  RAW == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (FX)
     ok = ok && vqlin::encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xq, (uint64_t)K, (uint64_t)M,
                                      (uint64_t)K * 2, 64, (uint32_t)bt, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -865,7 +905,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   a.M = M; a.N = N; a.K = K; a.bt = bt; a.nkb = nkb; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
   {
     const uint32_t bt_pad = (uint32_t)((bt + 31) / 32 * 32);
-    a.chunk_kb = chunked ? 1024 / kb_codes : 0;
+    a.chunk_kb = chunked ? exact_ch / kb_codes : 0;
     a.d1_col = bt_pad;
     a.r_col = 2 * bt_pad;
   }
@@ -903,6 +943,13 @@ vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const vo
   if (M == 0 || N == 0) return VQLIN_OK;
   if (bits == 4) return launch_bits<4>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
   return launch_bits<8>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
+}
+
+vqlin_status launch_int_gemm_w4a8(const void* xq, const float* sx, const void* wq, const float* sw,
+                                  const uint16_t* bias, uint16_t* Y, int32_t* acc, int M, int N, int K, int* status,
+                                  cudaStream_t st) {
+  if (M == 0 || N == 0) return VQLIN_OK;
+  return launch_bits<8, false, 128, true>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
 }
 
 vqlin_status launch_int_gemm_static_act(const uint16_t* X, const float* static_scale, int hb, const void* wq,

@@ -188,9 +188,10 @@ vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
                              "act_hadamard_quant");
 }
 
+// bits: 4 (W4A4), 8 (W8A8); w4a8: int4 weights against int8 activations
 static vqlin_status linear_int(int bits, const void* xq, const float* sx, const void* wq, const float* sw,
                                const uint16_t* bias, uint16_t* Y, int32_t* acc, int M, int N, int K,
-                               void* stream) {
+                               void* stream, bool w4a8 = false) {
   REQUIRE(M >= 0 && N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
   const int kmul = bits == 4 ? 128 : 64;
   const int kmax = bits == 4 ? vqlin::kGemmW4MaxK : vqlin::kGemmW8MaxK;
@@ -207,6 +208,9 @@ static vqlin_status linear_int(int bits, const void* xq, const float* sx, const 
   }
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
+  if (w4a8)
+    return vqlin::launch_int_gemm_w4a8(xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
+                                       static_cast<cudaStream_t>(stream));
   return vqlin::launch_int_gemm(bits, xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
                                 static_cast<cudaStream_t>(stream));
 }
@@ -219,6 +223,17 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
 vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                const uint16_t* bias, uint16_t* Y, int M, int N, int K, void* stream) {
   return linear_int(8, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream);
+}
+
+vqlin_status vqlin_linear_w4a8(const uint16_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                               const uint16_t* bias, uint16_t* Y, int M, int N, int K, void* stream) {
+  return linear_int(8, xq, sx, wq, sw, bias, Y, nullptr, M, N, K, stream, true);
+}
+
+vqlin_status vqlin_debug_gemm_w4a8_s32(const uint16_t* xq, const uint8_t* wq, int32_t* acc, int M, int N, int K,
+                                       void* stream) {
+  REQUIRE_PTR(acc);
+  return linear_int(8, xq, nullptr, wq, nullptr, nullptr, nullptr, acc, M, N, K, stream, true);
 }
 
 vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale, int hadamard_block,

@@ -143,6 +143,21 @@ vqlin_status vqlin_linear_w4a4(const uint8_t* xq, const float* sx, const uint8_t
                                int M, int N, int K, void* stream);
 
 /*
+ * W4A8 projection (QuantVLA's setting: int4 weights, int8 per-token
+ * activations): Y = bf16( (sum_k xq[m,k] * wq[n,k]) * sx[m] * sw[n] + bias[n] )
+ * with the int32 sum exact.  xq: int8 activation codes [M, K] uint16 (as for
+ * vqlin_linear_w8a8, from vqlin_act_hadamard_quant with bits 8); wq: int4
+ * weight codes [N, K/2] (as for vqlin_linear_w4a4, from
+ * vqlin_quantize_weights_rtn with bits 4); the other arguments as for
+ * vqlin_linear_w4a4.  Runs on the f16 tensor cores (exact subnormal operands;
+ * float32 partial sums of at most 16384 channels stay below 2^24 and are added
+ * up in int32).  Requires K % 64 == 0 and K <= 65536.
+ */
+vqlin_status vqlin_linear_w4a8(const uint16_t* xq, const float* sx, const uint8_t* wq,
+                               const float* sw, const uint16_t* bias, uint16_t* Y,
+                               int M, int N, int K, void* stream);
+
+/*
  * W4A4 projection with the activations quantized on chip at a static scale
  * (Omega-QVLA "Scalatura delle Attivazioni DiT per Passo": per-step
  * precomputed activation scales; FoldQuantVLA abstract: block Hadamard
@@ -187,6 +202,11 @@ vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint
  */
 vqlin_status vqlin_linear_bf16_ref(const uint16_t* X, const uint16_t* W, const uint16_t* bias,
                                    uint16_t* Y, int M, int N, int K, void* stream);
+
+/* Test entry point: the int32 accumulators of the W4A8 GEMM (codes as for
+ * vqlin_linear_w4a8) into acc [M, N] int32, caller-owned. */
+vqlin_status vqlin_debug_gemm_w4a8_s32(const uint16_t* xq, const uint8_t* wq, int32_t* acc,
+                                       int M, int N, int K, void* stream);
 
 /*
  * Test entry point: the integer GEMM of vqlin_linear_w4a4 (bits 4) or

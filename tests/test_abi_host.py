@@ -76,6 +76,10 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a4(A, None, A, A, None, A, 16, 16, 256, None) == INVALID
     assert lib.vqlin_linear_w4a4(A + 1, A, A, A, None, A, 16, 16, 256, None) == MISALIGNED
     assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 0, 16, 256, None) == OK
+    assert lib.vqlin_linear_w4a8(A, A, A, A, None, A, 16, 16, 96, None) == UNSUPPORTED       # K % 64
+    assert lib.vqlin_linear_w4a8(A, None, A, A, None, A, 16, 16, 128, None) == INVALID       # null sx
+    assert lib.vqlin_linear_w4a8(A + 2, A, A, A, None, A, 16, 16, 128, None) == MISALIGNED
+    assert lib.vqlin_debug_gemm_w4a8_s32(A, A, None, 16, 16, 128, None) == INVALID          # null acc
     f = lib.vqlin_linear_w4a4_static
     assert f(A, A, 128, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED    # K % 128
     assert f(A, A, 32, A, A, None, A, 16, 16, 256, None) == INVALID         # block size

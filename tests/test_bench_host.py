@@ -79,5 +79,6 @@ def test_work_formulas_match_the_scope_table():
     assert stack.work_of(("linear_w8a8", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N)
     assert stack.work_of(("linear_w4a16", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // 128
                                                         + 2 * M * N)
+    assert stack.work_of(("linear_w4a8", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N)
     assert stack.work_of(("act_quant_static", 4, M, K)) == (0, 2 * M * K + M * K + 4 * M)
     assert stack.work_of(("act_quant", 8, M, K)) == (0, 2 * M * K + 2 * M * K + 4 * M)

@@ -301,6 +301,76 @@ def test_int_gemm_extremes(bits, K):
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
 
 
+W4A8_SHAPES = [(1, 8, 64), (16, 256, 256), (17, 200, 384), (50, 1024, 1024), (129, 257, 512), (816, 256, 2048),
+               (50, 1024, 4096), (64, 256, 16384), (816, 512, 16384), (33, 200, 20480), (2, 128, 32768)]
+
+
+@pytest.mark.parametrize("shape", W4A8_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_int_gemm_w4a8_bit_exact(shape):
+    # int4 weight codes (packed as for W4A4) against int8 activation codes
+    # (encoded as for W8A8); beyond 16384 channels the sums are chunked
+    M, N, K = shape
+    xq = random_codes((M, K), -127, 127, seed=11, tags=("x", 48))
+    wq = random_codes((N, K), -7, 7, seed=12, tags=("w", 48))
+    acc = Guarded((M, N), torch.int32)
+    vq.debug_gemm_w4a8_s32(encode_act(xq, 8), pack_codes(wq, 4), K, out=acc.t)
+    acc.check()
+    vq.get_last_device_error()
+    np.testing.assert_array_equal(acc.t.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
+
+
+@pytest.mark.parametrize("K", [16384, 65536])
+def test_int_gemm_w4a8_extremes(K):
+    # all-maximum codes: 7 x 127 x K reaches 2^25.8 at K = 65536, beyond the
+    # 2^24 float32 range, exact only through the chunked int32 sums
+    M, N = 4, 16
+    xq = np.full((M, K), -127, np.int8)
+    wq = np.full((N, K), -7, np.int8)
+    wq[1::2, ::2] = 7
+    wq[2, K // 2:] = 1
+    acc = vq.debug_gemm_w4a8_s32(encode_act(xq, 8), pack_codes(wq, 4), K)
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), o.int_gemm(xq, wq))
+
+
+W4A8_LINEAR_CASES = [
+    # (M, N, K, hb, dist, outlier_frac, outlier_scale)
+    (16, 256, 256, 64, "normal", 4 / 256, 20.0),
+    (1, 1024, 1024, 128, "normal", 0.0, 1.0),
+    (50, 1024, 1024, 128, "normal", 0.0, 1.0),
+    (816, 256, 2048, 128, "student_t4", 0.01, 30.0),
+    (64, 512, 4096, 128, "normal", 0.005, 50.0),
+    (17, 300, 20480, 128, "normal", 0.005, 50.0),
+]
+
+
+@pytest.mark.parametrize("case", W4A8_LINEAR_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}")
+def test_linear_w4a8_end_to_end(case):
+    M, N, K, hb, dist, frac, sc = case
+    Xb = activations(M, K, dist=dist, n_outliers=int(round(frac * K)), outlier_scale=sc, seed=24)
+    Wb = weights(N, K, seed=25)
+    bias = weights(1, N, std=0.5, seed=26)[0]
+    X, W = to_dev_bf16(Xb), to_dev_bf16(Wb)
+    wq, sw = vq.quantize_weights_rtn(W, 4, True, 0, hb)
+    xq, sx = vq.act_hadamard_quant(X, 8, hb)
+    yg = Guarded((M, N), torch.bfloat16)
+    vq.linear_w4a8(xq, sx, wq, sw, to_dev_bf16(bias), out=yg.t)
+    yg.check()
+    ref = o.linear_quantized(Xb, Wb, 4, hb, bias_bits=bias, act_bits=8)
+    assert rel_fro(bf16_bits(yg.t), ref["y"]) <= 1e-3
+
+
+def test_linear_w4a8_with_oracle_codes():
+    M, N, K = 33, 264, 1024
+    Xb = activations(M, K, n_outliers=10, outlier_scale=20, seed=34)
+    Wb = weights(N, K, seed=35)
+    bias = weights(1, N, std=0.5, seed=36)[0]
+    ref = o.linear_quantized(Xb, Wb, 4, 128, bias_bits=bias, act_bits=8)
+    y = vq.linear_w4a8(encode_act(ref["xq"], 8), torch.from_numpy(ref["sx"]).to(DEV), pack_codes(ref["wq"], 4),
+                       torch.from_numpy(ref["sw"]).to(DEV), to_dev_bf16(bias))
+    ulp = np.abs(bf16_bits(y).astype(np.int64) - ref["y"].astype(np.int64))
+    assert ulp.max() <= 1 and (ulp > 0).mean() < 0.01
+
+
 @pytest.mark.parametrize("bits", [4, 8])
 def test_int_gemm_bounded_wait_reports_timeout(bits):
     # the producer withholds every tile load: the consumers' waits run out
