@@ -99,7 +99,7 @@ using vqlin::fail;
 
 extern "C" {
 
-int vqlin_version(void) { return 400; }
+int vqlin_version(void) { return 500; }
 
 const char* vqlin_status_string(vqlin_status s) {
   switch (s) {
