@@ -5,7 +5,9 @@
 //
 // Method: "FoldQuantVLA" abstract (W4A4 projections executed natively in
 // integers after per-token activation and per-channel weight quantization;
-// attention-output and FFN-down projections kept at W8A8).
+// attention-output and FFN-down projections kept at W8A8); W4A8 is the
+// setting evaluated in the "QuantVLA: Scale-Calibrated Post-Training
+// Quantization for Vision-Language-Action Models" summary (section 4).
 //
 // sm_103a has no integer tcgen05 MMA, so the integer codes ride in floating
 // point operands whose products and sums are exact:
