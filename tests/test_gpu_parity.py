@@ -475,3 +475,21 @@ def test_linear_bf16_ref(MNK):
 
 def test_no_device_error_recorded():
     vq.get_last_device_error()
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_output_scale_folds_ride_in_the_weight_scales(bits):
+    # attention-temperature / output-head factors folded into the weight
+    # scales before the call: the GEMMs take them as ordinary weight scales
+    from oracle import scale_folding as sf
+    M, N, K, hb = 50, 256, 1024, 128
+    Xb = activations(M, K, n_outliers=5, outlier_scale=20, seed=71)
+    Wb = weights(N, K, seed=72)
+    f = sf.head_factors(np.array([1.0, 1.3, 0.75, 1.1]), N // 4)
+    wq, sw = vq.quantize_weights_rtn(to_dev_bf16(Wb), bits, True, 0, hb)
+    sw_folded = sw * torch.from_numpy(f.astype(np.float32)).to(DEV)
+    xq, sx = vq.act_hadamard_quant(to_dev_bf16(Xb), bits, hb)
+    fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
+    y = fn(xq, sx, wq, sw_folded)
+    ref = sf.linear_quantized_scaled(Xb, Wb, bits, hb, out_factor=f)
+    assert rel_fro(bf16_bits(y), ref["y"]) <= 1e-3
