@@ -347,14 +347,11 @@ class ControlStepStack:
                 for gi, g in enumerate(self.exp_groups):
                     b, w, x = self.exp_buf[gi], self.exp_w[l][gi], self.exp_x[t][l][gi]
                     s = self.static[t, l, gi:gi + 1]
-                    # the activation kernel, then the GEMM: at 50 tokens this beats the GEMM that
-                    # quantizes on chip (linear_w4a4_static), whose every CTA re-quantizes its
-                    # activation tile
-                    self._go(("act_quant_static", 4, self.M_exp, g["K"]),
-                             lambda b=b, x=x, s=s: vq.act_hadamard_quant(x, 4, self.hb, static_scale=s,
-                                                                         q_out=b["xq"], scale_out=b["sx"]))
-                    self._go(("linear_w4a4", self.M_exp, g["N"], g["K"]),
-                             lambda b=b, w=w: vq.linear_w4a4(b["xq"], b["sx"], w["q4"], w["s4"], out=b["y4"]))
+                    # one launch: the GEMM rotates and quantizes its activations on chip (once per
+                    # cluster, the codes exchanged through xq) at the step's static scale
+                    self._go(("linear_w4a4_static", self.M_exp, g["N"], g["K"]),
+                             lambda b=b, w=w, x=x, s=s: vq.linear_w4a4_static(x, s, w["q4"], w["s4"], self.hb,
+                                                                             out=b["y4"], xq_out=b["xq"]))
 
     def expert_w4a16(self):
         vq = self.vq
@@ -773,7 +770,8 @@ def run_shape(args):
         st = torch.full((1,), 0.5, device=dev)
         mk = lambda: dict(wq=rand_codes(N, K, 4), sw=torch.rand(N, generator=g, device=dev))  # noqa: E731
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        run = lambda d: vq.linear_w4a4_static(X, st, d["wq"], d["sw"], 128, out=y)  # noqa: E731
+        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        run = lambda d: vq.linear_w4a4_static(X, st, d["wq"], d["sw"], 128, out=y, xq_out=xq)  # noqa: E731
     elif kind == "linear_w4a16":
         per = N * K // 2
         flops, nbytes = 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // group + 2 * M * N

@@ -29,7 +29,7 @@ __all__ = [
     "VqlinError", "load", "LIB_PATH",
     "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w4a4_static", "linear_w8a8",
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
-    "debug_gemm_withheld_loads",
+    "debug_gemm_withheld_loads", "measure_mma_rate",
     "get_last_device_error",
 ]
 
@@ -124,11 +124,12 @@ def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
 
 
 def linear_w4a4_static(X, static_scale, wq, sw, hadamard_block: int = 128, bias=None, out=None,
-                       stream=None):
+                       xq_out=None, stream=None):
     """W4A4 with the activations quantized inside the GEMM at a static scale:
     the same Y as act_hadamard_quant(X, 4, hadamard_block, static_scale) followed
     by linear_w4a4.  X bf16 [M, K], static_scale float32 (one element), wq uint8
-    [N, K/2]."""
+    [N, K/2].  xq_out (uint8 [M, K], allocated if None) receives the activation
+    codes; the kernel also uses it to share them among its CTAs."""
     _need(X, "X", torch.bfloat16, 2)
     _need(static_scale, "static_scale", torch.float32)
     _need(wq, "wq", torch.uint8, 2)
@@ -141,8 +142,13 @@ def linear_w4a4_static(X, static_scale, wq, sw, hadamard_block: int = 128, bias=
         _need(bias, "bias", torch.bfloat16, 1)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if xq_out is None:
+        xq_out = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+    _need(xq_out, "xq_out", torch.uint8, 2)
+    if tuple(xq_out.shape) != (M, K):
+        raise ValueError("xq_out must be [M, K]")
     check(_lib.vqlin_linear_w4a4_static(_ptr(X), _ptr(static_scale), hadamard_block, _ptr(wq), _ptr(sw),
-                                        _ptr(bias), _ptr(out), M, N, K, _stream(stream)),
+                                        _ptr(bias), _ptr(out), _ptr(xq_out), M, N, K, _stream(stream)),
           "vqlin_linear_w4a4_static")
     return out
 
@@ -232,3 +238,21 @@ def debug_gemm_withheld_loads(bits: int, xq, wq, K: int, limit_ns: int, out=None
                                                ctypes.c_uint64(limit_ns), _stream(stream)),
           "vqlin_debug_gemm_withheld_loads")
     return out
+
+
+def measure_mma_rate(kind: str, n: int, a_in_tmem: bool = True, accumulators: int = 1, issuers: int = 1,
+                     iters: int = 4096, ctas=None, device=None, stream=None):
+    """Dense rate of one tcgen05 MMA kind on this GPU ("e4m3": kind::f8f6f4,
+    "bf16": kind::f16): (TFLOP/s over all CTAs, SM clocks per 128 x n x K MMA),
+    with the MMAs spread over `accumulators` independent accumulators issued
+    by `issuers` warps."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if ctas is None:
+        ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.empty((ctas,), dtype=torch.int64, device=dev)
+    tf, cpm = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    k = {"e4m3": 0, "bf16": 1}[kind]
+    check(_lib.vqlin_measure_mma_rate(k, int(a_in_tmem), n, accumulators, issuers, iters, ctas, _ptr(cyc),
+                                      ctypes.byref(tf),
+                                      ctypes.byref(cpm), _stream(stream)), "vqlin_measure_mma_rate")
+    return tf.value, cpm.value

@@ -32,7 +32,7 @@ SIGNATURES = {
     "vqlin_quantize_weights_rtn": (_i, [_p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p]),
     "vqlin_act_hadamard_quant": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p]),
     "vqlin_linear_w4a4": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
-    "vqlin_linear_w4a4_static": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "vqlin_linear_w4a4_static": (_i, [_p, _p, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w8a8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w4a8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_debug_gemm_w4a8_s32": (_i, [_p, _p, _p, _i, _i, _i, _p]),
@@ -40,6 +40,8 @@ SIGNATURES = {
     "vqlin_linear_bf16_ref": (_i, [_p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_debug_gemm_s32": (_i, [_i, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_debug_gemm_withheld_loads": (_i, [_i, _p, _p, _p, _i, _i, _i, ctypes.c_uint64, _p]),
+    "vqlin_measure_mma_rate": (_i, [_i, _i, _i, _i, _i, _i, _i, _p, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double), _p]),
 }
 
 _lib = None

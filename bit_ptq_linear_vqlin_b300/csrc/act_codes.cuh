@@ -90,4 +90,49 @@ __device__ __forceinline__ void quantize_chunk(const float (&v)[8], float s, flo
   }
 }
 
+// The same codes from the hardware's float -> e4m3 / f16 conversions, for
+// rotated activations: c * 2^-9 (int4) and c * 2^-24 (int8) are the
+// subnormals of those formats, so converting clamp(v * inv_s, +-qmax) scaled
+// by that power of two rounds half to even straight into the operand
+// encoding, two codes per instruction (the exact path above spends a round
+// and a float -> integer conversion on every code, on a conversion unit a
+// quarter as wide as the arithmetic units).  The decision is taken on the
+// float32 product v * inv_s, which differs from the IEEE quotient v / s only
+// within 2^-22 (relative) of a half-integer.  k = inv_s * 2^-9 (int4) or
+// inv_s * 2^-24 (int8).  A zero is encoded +0.
+template <int BITS>
+__device__ __forceinline__ void quantize_chunk_fast(const float (&v)[8], float k, uint32_t (&w)[4]) {
+  constexpr float lim = BITS == 4 ? 7.0f / 512.0f : 127.0f / 16777216.0f;  // qmax times the unit
+  float c[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) c[e] = fminf(fmaxf(v[e] * k, -lim), lim);
+  if (BITS == 4) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t lo, hi;
+      asm("{\n\t.reg .b16 a, b;\n\t"
+          "cvt.rn.satfinite.e4m3x2.f32 a, %3, %2;\n\t"
+          "cvt.rn.satfinite.e4m3x2.f32 b, %5, %4;\n\t"
+          "cvt.u32.u16 %0, a;\n\tcvt.u32.u16 %1, b;\n\t}"
+          : "=r"(lo), "=r"(hi)
+          : "f"(c[4 * h]), "f"(c[4 * h + 1]), "f"(c[4 * h + 2]), "f"(c[4 * h + 3]));
+      uint32_t x = lo | (hi << 16);
+      // clear the sign of zero codes: bit 7 of (b & 0x7F) + 0x7F is set iff b & 0x7F != 0
+      const uint32_t mag = x & 0x7F7F7F7Fu;
+      x = mag | (x & (mag + 0x7F7F7F7Fu) & 0x80808080u);
+      w[h] = x;
+    }
+    w[2] = w[3] = 0;
+  } else {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t x;
+      asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(x) : "f"(c[2 * h]), "f"(c[2 * h + 1]));
+      const uint32_t mag = x & 0x7FFF7FFFu;
+      x = mag | (x & (mag + 0x7FFF7FFFu) & 0x80008000u);
+      w[h] = x;
+    }
+  }
+}
+
 }  // namespace vqlin_dev

@@ -94,8 +94,10 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
     s = __fdiv_rn(amax, (float)qmax);
   }
   if (!row_ok) return;
-  if (ut == 0) S[m] = s;
+  if (ut == 0 && S != nullptr) S[m] = s;
   const float inv_s = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  // rotated activations: the hardware conversions (see quantize_chunk_fast)
+  const float kq = inv_s * (BITS == 4 ? 1.0f / 512.0f : 1.0f / 16777216.0f);
 
 #pragma unroll
   for (int i = 0; i < UPT; ++i) {
@@ -105,7 +107,10 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t w[4];
-      quantize_chunk<BITS>(v[i][j], s, inv_s, w);
+      if (HB > 0)
+        quantize_chunk_fast<BITS>(v[i][j], kq, w);
+      else
+        quantize_chunk<BITS>(v[i][j], s, inv_s, w);
       const size_t ch = (size_t)g * G + (l + LPG * j) * 8;  // first channel of the chunk
       if (BITS == 4) {
         *reinterpret_cast<uint2*>(Q + (size_t)m * K + ch) = make_uint2(w[0], w[1]);

@@ -59,6 +59,11 @@ vqlin_status launch_int_gemm(int bits, const void* xq, const float* sx, const vo
 vqlin_status launch_int_gemm_w4a8(const void* xq, const float* sx, const void* wq, const float* sw,
                                   const uint16_t* bias, uint16_t* Y, int32_t* acc, int M, int N, int K, int* status,
                                   cudaStream_t st);
+// W4A4 GEMM of activation codes quantized at one static scale (*static_scale
+// applies to every token).
+vqlin_status launch_int_gemm_static_scale(const void* xq, const float* static_scale, const void* wq, const float* sw,
+                                          const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
+                                          cudaStream_t st);
 // W4A4 GEMM whose activations arrive as bf16 and are quantized on chip (block
 // Hadamard of hb = 64 or 128 channels, one static scale) instead of by a
 // separate activation kernel.
@@ -78,6 +83,21 @@ vqlin_status launch_w4a16_tc(const uint16_t* X, const uint8_t* wq, const uint16_
                              const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
                              int M, int N, int K, int* status, cudaStream_t st);
 constexpr int kW4a16GemvMaxM = 4;
+
+// Few-token W4A4 (lowlat_tcgen05.cu): every operand of a CTA's K range stays
+// on chip; at most 8 k-blocks of 128 channels per CTA and 16 CTAs along K.
+constexpr int kLowlatMaxM = 128;
+constexpr int kLowlatMaxK = 16384;
+// Static-scale W4A4 whose activations are rotated and quantized on chip, once
+// per cluster, into the code buffer xq_ws [M, K] (bytes, the activation
+// kernel's encoding), which the CTAs then read back; any M, K <= kLowlatMaxK.
+vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_scale, int hb, uint8_t* xq_ws,
+                                       const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
+                                       int N, int K, int* status, cudaStream_t st);
+// The same kernel fed with the activation kernel's codes and per-token scales.
+vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                                      const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
+                                      cudaStream_t st);
 
 // Largest K each kernel supports (host-side shape checks).
 constexpr int kActQuantMaxK = 65536;

@@ -98,6 +98,7 @@ struct QgemmArgs {
   int tma_store;         // unsplit K: stage the bf16 tile and store it with TMA
   int rows_per;          // split K: output channels each cluster rank owns
   const float* static_scale;  // on-chip activation quantization: the static scale (one float)
+  int sx_step;           // 1: per-token scales sx[m]; 0: one scale sx[0] for every token
 };
 
 // Expands 8 packed bytes into 4 words of A operand in channel order.
@@ -210,7 +211,6 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  if (tid == 0) pdl_trigger();
 
   if (warp == 0) {
     // lanes 1..31 stage the epilogue's per-token and per-channel scales and the
@@ -231,7 +231,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < 9; ++j) {
           const int i = lane - 1 + 31 * j;
-          xv[j] = i < bt && m0 + i < a.M ? (FX ? xs : __ldg(a.sx + m0 + i)) : 0.0f;
+          xv[j] = i < bt && m0 + i < a.M ? (FX ? xs : __ldg(a.sx + (size_t)(m0 + i) * a.sx_step)) : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < 5; ++j) {
@@ -279,6 +279,9 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
           tma_load_2d(base + (size_t)i * stage_bytes + b_bytes, &tmW, (kb0 + i) * RAW, n0, &full[i]);
         }
         pdl_wait();
+        // the next kernel may prepare once this one works; an earlier trigger
+        // lets a chain of launches prefetch weights all at once
+        pdl_trigger();
         for (int i = 0; i < pre; ++i) {
           load_x(base + (size_t)i * stage_bytes, kb0 + i, &full[i]);
           ++issued;
@@ -302,6 +305,7 @@ qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
         }
       } else {
         pdl_wait();
+        pdl_trigger();
       }
       // copies still in flight complete before the CTA may exit
       for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
@@ -752,7 +756,7 @@ size_t smem_bytes(int bt, int stages, bool fx, int raw) {
 template <int BITS, bool FX = false, int HB = 128, bool W4 = false>
 vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const float* sw, const uint16_t* bias,
                          uint16_t* Y, int32_t* acc, int M, int N, int K, int* status, int withhold,
-                         uint64_t limit_ns, cudaStream_t st) {
+                         uint64_t limit_ns, cudaStream_t st, int sx_step = 1) {
   constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
   const auto kern = qgemm_kernel<BITS, FX, HB, W4>;
   constexpr int RAW = (BITS == 8 && W4) ? 32 : kRawRow;
@@ -912,7 +916,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     a.r_col = 2 * bt_pad;
   }
   a.wait_limit_ns = limit_ns; a.withhold_loads = withhold;
-  a.tma_store = tma_store ? 1 : 0; a.rows_per = rows_per;
+  a.tma_store = tma_store ? 1 : 0; a.rows_per = rows_per; a.sx_step = sx_step;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, S);
@@ -952,6 +956,13 @@ vqlin_status launch_int_gemm_w4a8(const void* xq, const float* sx, const void* w
                                   cudaStream_t st) {
   if (M == 0 || N == 0) return VQLIN_OK;
   return launch_bits<8, false, 128, true>(xq, sx, wq, sw, bias, Y, acc, M, N, K, status, 0, kWaitLimitNs, st);
+}
+
+vqlin_status launch_int_gemm_static_scale(const void* xq, const float* static_scale, const void* wq, const float* sw,
+                                          const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
+                                          cudaStream_t st) {
+  if (M == 0 || N == 0) return VQLIN_OK;
+  return launch_bits<4>(xq, static_scale, wq, sw, bias, Y, nullptr, M, N, K, status, 0, kWaitLimitNs, st, 0);
 }
 
 vqlin_status launch_int_gemm_static_act(const uint16_t* X, const float* static_scale, int hb, const void* wq,

@@ -51,7 +51,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete, for at most
 // `limit_ns` nanoseconds.  Gives up early when *abort becomes non-zero (another
-// role of the CTA gave up).  Returns true when the phase completed.
+// role of the CTA gave up).  Returns true when the phase completed.  (A
+// suspend-time hint on the test would take the waiting warp off the issue
+// slots, but on B300 its wake-up after the phase completes is late enough to
+// lengthen a latency-bound kernel, so the test spins; kernels keep the number
+// of spinning warps small instead.)
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -211,6 +211,10 @@ static vqlin_status linear_int(int bits, const void* xq, const float* sx, const 
   if (w4a8)
     return vqlin::launch_int_gemm_w4a8(xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
                                        static_cast<cudaStream_t>(stream));
+  // few tokens: the kernel that keeps every operand of its K range on chip
+  if (bits == 4 && acc == nullptr && M <= vqlin::kLowlatMaxM && K <= vqlin::kLowlatMaxK)
+    return vqlin::launch_w4a4_codes_lowlat(static_cast<const uint8_t*>(xq), sx, static_cast<const uint8_t*>(wq), sw,
+                                           bias, Y, M, N, K, status, static_cast<cudaStream_t>(stream));
   return vqlin::launch_int_gemm(bits, xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
                                 static_cast<cudaStream_t>(stream));
 }
@@ -237,20 +241,27 @@ vqlin_status vqlin_debug_gemm_w4a8_s32(const uint16_t* xq, const uint8_t* wq, in
 }
 
 vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale, int hadamard_block,
-                                      const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
-                                      int N, int K, void* stream) {
+                                      const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y,
+                                      uint8_t* xq_out, int M, int N, int K, void* stream) {
   REQUIRE(M >= 0 && N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
   REQUIRE(hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
           "hadamard_block must be 64 or 128 (got %d)", hadamard_block);
   REQUIRE(K % 128 == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 128", K);
   REQUIRE(K <= vqlin::kGemmW4MaxK, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K, vqlin::kGemmW4MaxK);
   if (M == 0 || N == 0) return VQLIN_OK;
-  REQUIRE_PTR(X); REQUIRE_PTR(static_scale); REQUIRE_PTR(wq); REQUIRE_PTR(sw); REQUIRE_PTR(Y);
-  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(Y);
+  REQUIRE_PTR(X); REQUIRE_PTR(static_scale); REQUIRE_PTR(wq); REQUIRE_PTR(sw); REQUIRE_PTR(Y); REQUIRE_PTR(xq_out);
+  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(Y); REQUIRE_ALIGNED(xq_out);
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
-  return vqlin::launch_int_gemm_static_act(X, static_scale, hadamard_block, wq, sw, bias, Y, M, N, K, status,
-                                           static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K <= vqlin::kLowlatMaxK)
+    return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, xq_out, wq, sw, bias, Y, M, N, K,
+                                            status, st);
+  // longer K: the activation kernel writes the codes, the throughput GEMM uses them
+  vqlin_status r = vqlin::check_launch(
+      vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st), "act_hadamard_quant");
+  if (r != VQLIN_OK) return r;
+  return vqlin::launch_int_gemm_static_scale(xq_out, static_scale, wq, sw, bias, Y, M, N, K, status, st);
 }
 
 vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int32_t* acc, int M, int N, int K,

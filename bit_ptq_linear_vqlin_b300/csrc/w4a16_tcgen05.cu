@@ -145,7 +145,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  if (tid == 0) pdl_trigger();
 
   float y[BT];
 #pragma unroll
@@ -162,6 +161,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         tma_load_2d(base + (size_t)i * kStageBytes + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
       }
       pdl_wait();
+      // the next kernel may prepare once this one works; an earlier trigger
+      // lets a chain of launches prefetch weights all at once
+      pdl_trigger();
       for (int i = 0; i < pre; ++i) {
         tma_load_2d(base + (size_t)i * kStageBytes, &tmX, (kb0 + i) * kKB, m0, &full[i]);
         ++issued;

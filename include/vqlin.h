@@ -162,18 +162,24 @@ vqlin_status vqlin_linear_w4a8(const uint16_t* xq, const float* sx, const uint8_
  * (Omega-QVLA "Scalatura delle Attivazioni DiT per Passo": per-step
  * precomputed activation scales; FoldQuantVLA abstract: block Hadamard
  * rotation and native integer execution).  Computes exactly what
- * vqlin_act_hadamard_quant(X, M, K, 4, hadamard_block, static_scale, xq, sx)
- * followed by vqlin_linear_w4a4(xq, sx, wq, sw, bias, Y, M, N, K) computes
- * (the same codes bit for bit, hence the same Y) in one kernel, without the
- * code matrix in memory.
+ * vqlin_act_hadamard_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, s)
+ * followed by vqlin_linear_w4a4(xq_out, s, wq, sw, bias, Y, M, N, K) computes
+ * (the same codes bit for bit, hence the same Y), in one kernel when
+ * K <= 16384.  The kernel rotates and quantizes each activation tile once per
+ * thread-block cluster, not once per CTA: the cluster's CTAs write the codes to
+ * xq_out, meet at a cluster barrier and read the codes of their K range back
+ * from L2.  So xq_out is both the code output and the kernel's exchange buffer.
  * X: bf16 [M, K]; static_scale: ONE device float (> 0, finite); hadamard_block
  * 64 or 128; wq, sw, bias, Y as for vqlin_linear_w4a4 (wq rotated with the same
- * block).  Requires K % 128 == 0 and K <= 65536.
+ * block); xq_out: [M, K] bytes, caller-owned, receives the activation codes in
+ * the int4 activation-code encoding (its previous contents are ignored).
+ * Requires K % 128 == 0 and K <= 65536 (beyond 16384 channels: the activation
+ * kernel, then the GEMM, two launches).
  */
 vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale,
                                       int hadamard_block, const uint8_t* wq, const float* sw,
-                                      const uint16_t* bias, uint16_t* Y, int M, int N, int K,
-                                      void* stream);
+                                      const uint16_t* bias, uint16_t* Y, uint8_t* xq_out,
+                                      int M, int N, int K, void* stream);
 
 /* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
  * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands;
@@ -227,6 +233,25 @@ vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int3
  */
 vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const void* wq, int32_t* acc,
                                              int M, int N, int K, uint64_t limit_ns, void* stream);
+
+/*
+ * Measurement entry point: the dense rate of one tensor-core MMA kind on this
+ * GPU, the roofline denominator of the projections (no passage of the pages
+ * defines it; they name no GPU figure).  kind 0: tcgen05.mma kind::f8f6f4 with
+ * e4m3 operands (K = 32 per instruction, the W4A4 GEMM); kind 1: kind::f16
+ * with bf16 operands (K = 16, the W4A16 / W8A8 / W4A8 GEMMs).  `ctas` CTAs (one
+ * per SM; 148 covers a B300) each issue iters x 4 back-to-back 128 x n x K
+ * MMAs on operands resident on chip (A in tensor memory if a_in_tmem, else in
+ * shared memory; n a multiple of 16 in [16, 256]) from `issuers` warps (1, 2
+ * or 4), spread over `accumulators` independent accumulation chains (1, 2 or
+ * 4, a multiple of issuers, accumulators * n <= 256).  cycles_dev: device buffer
+ * of `ctas` int64, caller-owned (per-CTA SM-clock spans).  Outputs (host):
+ * *tflops = flops / event time; *cycles_per_mma = average SM clocks per MMA
+ * instruction of the CTA.  Synchronous (waits for the stream).
+ */
+vqlin_status vqlin_measure_mma_rate(int kind, int a_in_tmem, int n, int accumulators, int issuers,
+                                    int iters, int ctas, long long* cycles_dev, double* tflops,
+                                    double* cycles_per_mma, void* stream);
 
 #ifdef __cplusplus
 }

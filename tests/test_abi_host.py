@@ -81,11 +81,13 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a8(A + 2, A, A, A, None, A, 16, 16, 128, None) == MISALIGNED
     assert lib.vqlin_debug_gemm_w4a8_s32(A, A, None, 16, 16, 128, None) == INVALID          # null acc
     f = lib.vqlin_linear_w4a4_static
-    assert f(A, A, 128, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED    # K % 128
-    assert f(A, A, 32, A, A, None, A, 16, 16, 256, None) == INVALID         # block size
-    assert f(A, None, 128, A, A, None, A, 16, 16, 256, None) == INVALID     # null scale
-    assert f(A + 2, A, 128, A, A, None, A, 16, 16, 256, None) == MISALIGNED
-    assert f(A, A, 128, A, A, None, A, 0, 16, 256, None) == OK              # empty: no-op
+    assert f(A, A, 128, A, A, None, A, A, 16, 16, 192, None) == UNSUPPORTED    # K % 128
+    assert f(A, A, 32, A, A, None, A, A, 16, 16, 256, None) == INVALID         # block size
+    assert f(A, None, 128, A, A, None, A, A, 16, 16, 256, None) == INVALID     # null scale
+    assert f(A, A, 128, A, A, None, A, None, 16, 16, 256, None) == INVALID     # null code buffer
+    assert f(A + 2, A, 128, A, A, None, A, A, 16, 16, 256, None) == MISALIGNED
+    assert f(A, A, 128, A, A, None, A, A + 8, 16, 16, 256, None) == MISALIGNED  # code buffer
+    assert f(A, A, 128, A, A, None, A, A, 0, 16, 256, None) == OK              # empty: no-op
     assert lib.vqlin_linear_w4a16(A, A, A, A, 96, None, A, 4, 16, 256, None) == INVALID
     assert lib.vqlin_linear_w4a16(A, A, A, A, 128, None, A, 4, 16, 192, None) == UNSUPPORTED
     assert lib.vqlin_linear_w4a16(A, A, A, None, 128, None, A, 4, 16, 256, None) == INVALID

@@ -198,9 +198,12 @@ def test_weight_quant_zero_row():
 
 
 STATIC_CASES = [
-    # (M, N, K, hb): the expert projections at 50 tokens, tails and both blocks
+    # (M, N, K, hb): the four expert projections at 50 tokens (q|k|v, o, gate|up,
+    # down), split K (4096, 16384), the two-launch path beyond 16384 channels,
+    # tails (N not a multiple of 128 or 8, padded clusters), several token tiles
     (50, 1024, 1024, 128), (50, 3072, 1024, 128), (50, 1024, 4096, 128), (50, 8192, 1024, 128),
     (1, 128, 128, 128), (16, 256, 256, 64), (33, 300, 2048, 64), (130, 264, 1024, 128), (816, 256, 2048, 128),
+    (7, 1000, 16384, 128), (5, 256, 20480, 128), (64, 1160, 1024, 64), (50, 2056, 3072, 128),
 ]
 
 
@@ -218,32 +221,49 @@ def test_linear_w4a4_static_scale(case):
     wq, sw = vq.quantize_weights_rtn(W, 4, True, 0, hb)
     st = torch.tensor([s], dtype=torch.float32, device=DEV)
     yg = Guarded((M, N), torch.bfloat16)
-    vq.linear_w4a4_static(X, st, wq, sw, hb, b, out=yg.t)
+    xg = Guarded((M, K), torch.uint8)
+    vq.linear_w4a4_static(X, st, wq, sw, hb, b, out=yg.t, xq_out=xg.t)
     yg.check()
+    xg.check()
     vq.get_last_device_error()
     y = bf16_bits(yg.t)
     assert rel_fro(y, ref["y"]) <= 1e-3
-    # the same codes as the activation kernel, so the same output bit for bit
+    # the codes it used are the activation kernel's codes, so Y is the two-kernel Y bit for bit
     xq, sx = vq.act_hadamard_quant(X, 4, hb, static_scale=st)
     check_act_codes(xq, sx, Xb, 4, hb, static_scale=s)
+    np.testing.assert_array_equal(xg.t.cpu().numpy(), xq.cpu().numpy())
     np.testing.assert_array_equal(y, bf16_bits(vq.linear_w4a4(xq, sx, wq, sw, b)))
 
 
-def test_linear_w4a4_static_scale_oracle_codes():
-    # with the oracle's codes (no rounding ties in this draw) the output is the
-    # oracle's within one bf16 ulp
-    M, N, K, hb = 50, 640, 1024, 128
-    Xb = activations(M, K, n_outliers=5, outlier_scale=20, seed=61)
+def _tie_free_draw(M, K, hb, seed0):
+    """The first seeded draw whose exact rotated activations lie at least 1e-5
+    (in units of the scale) away from every rounding tie at its own calibrated
+    static scale: far beyond the float32 error of the GPU's transform, so every
+    code is unambiguous (searched on the oracle)."""
+    for seed in range(seed0, seed0 + 200):
+        Xb = activations(M, K, n_outliers=5, outlier_scale=20, seed=seed)
+        s = o.calibrate_static_scale([Xb], 4, hb)
+        q = o.rotated_f64(Xb, hb) / np.float64(s)
+        if np.min(np.abs(np.abs(q - np.floor(q)) - 0.5)) > 1e-5:
+            return Xb, s
+    raise AssertionError("no tie-free draw among 200 seeds")
+
+
+@pytest.mark.parametrize("MNK", [(16, 640, 1024), (50, 640, 1024), (16, 384, 4096)])
+def test_linear_w4a4_static_scale_oracle_codes(MNK):
+    # a draw with no rounding ties: the on-chip codes equal the oracle's and the
+    # output is the oracle's within one bf16 ulp
+    M, N, K = MNK
+    hb = 128
+    Xb, s = _tie_free_draw(M, K, hb, 61)
     Wb = weights(N, K, seed=62)
-    s = o.calibrate_static_scale([Xb], 4, hb)
     ref = o.linear_quantized(Xb, Wb, 4, hb, static_scale=s)
     X = to_dev_bf16(Xb)
     st = torch.tensor([s], dtype=torch.float32, device=DEV)
-    xq, sx = vq.act_hadamard_quant(X, 4, hb, static_scale=st)
-    if not np.array_equal(decode_act(xq, 4), ref["xq"]):
-        pytest.skip("a rounding tie in this draw")
+    xq = torch.empty((M, K), dtype=torch.uint8, device=DEV)
     y = vq.linear_w4a4_static(X, st, torch.from_numpy(o.pack_int4(ref["wq"])).to(DEV),
-                              torch.from_numpy(ref["sw"]).to(DEV), hb)
+                              torch.from_numpy(ref["sw"]).to(DEV), hb, xq_out=xq)
+    np.testing.assert_array_equal(decode_act(xq, 4), ref["xq"])
     ulp = np.abs(bf16_bits(y).astype(np.int64) - ref["y"].astype(np.int64))
     assert ulp.max() <= 1 and (ulp > 0).mean() < 0.01
 
