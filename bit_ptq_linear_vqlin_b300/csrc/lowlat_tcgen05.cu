@@ -666,3 +666,85 @@ vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const 
 }
 
 }  // namespace vqlin
+
+// ------------------------------------------- the projection that allocates nothing
+//
+// vqlin_linear_w4a4_static needs a caller-provided code buffer of M x K bytes,
+// through which the CTAs of a cluster share the activation codes.  Some
+// callers cannot provide one: code running while a CUDA graph is being
+// captured (where a device allocation is refused), hosts that hand a plugin
+// fixed buffers and forbid it any allocation of its own, and runtimes whose
+// memory is managed by someone else.  For them this entry point keeps the
+// exchange buffer in a fixed array of device memory that belongs to the
+// library: every GPU that loads the library reserves it until the process
+// exits, and every call on that GPU shares it.
+
+namespace {
+
+// Largest M x K (activation codes, one byte each) the array holds: 1 MiB, e.g.
+// 64 tokens x 16384 channels or 256 tokens x 4096 channels.
+constexpr size_t kNoAllocCodeBytes = size_t(1) << 20;
+
+// The exchange buffer.  In host code this name is not a device address; the
+// kernel gets the address that cudaGetSymbolAddress returns for the current
+// device.
+static __device__ __align__(256) uint8_t g_noalloc_codes[kNoAllocCodeBytes];
+
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[64] = {};
+
+// The device address of the array on the current device, looked up once per
+// device (with that device current).
+vqlin_status noalloc_codes_ptr(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return vqlin::fail(VQLIN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return vqlin::fail(VQLIN_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_codes);
+    if (e != cudaSuccess)
+      return vqlin::fail(VQLIN_ERR_CUDA, "cudaGetSymbolAddress(code array): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return VQLIN_OK;
+}
+
+}  // namespace
+
+extern "C" vqlin_status vqlin_linear_w4a4_static_noalloc(const uint16_t* X, const float* static_scale,
+                                                         int hadamard_block, const uint8_t* wq, const float* sw,
+                                                         const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                                         void* stream) {
+  if (M < 0 || N < 0 || K <= 0) return vqlin::fail(VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
+  if (hadamard_block != 64 && hadamard_block != 128)
+    return vqlin::fail(VQLIN_ERR_INVALID_ARG, "hadamard_block must be 64 or 128 (got %d)", hadamard_block);
+  if (K % 128 != 0 || K > vqlin::kGemmW4MaxK)
+    return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d must be a multiple of 128 and at most %d", K,
+                       vqlin::kGemmW4MaxK);
+  if ((size_t)M * (size_t)K > kNoAllocCodeBytes)
+    return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE,
+                       "M x K = %d x %d activation codes exceed the library's fixed %zu-byte code array "
+                       "(use vqlin_linear_w4a4_static with a buffer of your own)",
+                       M, K, kNoAllocCodeBytes);
+  if (M == 0 || N == 0) return VQLIN_OK;
+  if (X == nullptr || static_scale == nullptr || wq == nullptr || sw == nullptr || Y == nullptr)
+    return vqlin::fail(VQLIN_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!vqlin::aligned16(X) || !vqlin::aligned16(wq) || !vqlin::aligned16(Y))
+    return vqlin::fail(VQLIN_ERR_MISALIGNED, "X, wq and Y must be 16-byte aligned");
+  int* status = vqlin::device_status_word();
+  if (status == nullptr) return vqlin::fail(VQLIN_ERR_CUDA, "no device status word");
+  uint8_t* codes = nullptr;
+  const vqlin_status r = noalloc_codes_ptr(&codes);
+  if (r != VQLIN_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the same dispatch as vqlin_linear_w4a4_static, the code buffer being the array
+  if (K <= vqlin::kLowlatMaxK)
+    return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, codes, wq, sw, bias, Y, M, N, K, status,
+                                            st);
+  const cudaError_t e = vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, codes, nullptr, st);
+  if (e != cudaSuccess) return vqlin::fail(VQLIN_ERR_CUDA, "act_hadamard_quant: %s", cudaGetErrorString(e));
+  return vqlin::launch_int_gemm_static_scale(codes, static_scale, wq, sw, bias, Y, M, N, K, status, st);
+}

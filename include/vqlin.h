@@ -181,6 +181,36 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
                                       const uint16_t* bias, uint16_t* Y, uint8_t* xq_out,
                                       int M, int N, int K, void* stream);
 
+/*
+ * The same projection as vqlin_linear_w4a4_static, for callers that cannot
+ * allocate device memory: code that runs while a CUDA graph is being captured
+ * (where an allocation is refused), plugins whose host hands them fixed
+ * buffers and forbids allocations of their own, runtimes whose memory someone
+ * else manages.  (It has no counterpart on the pages; it changes where the
+ * kernel's exchange buffer lives, not what it computes.)
+ *
+ * Instead of a caller's code buffer it uses a fixed array of device memory
+ * that belongs to the library: 1 MiB, reserved on every GPU that loads the
+ * library until the process exits.  So M x K must be at most 1048576 (e.g. 64
+ * tokens x 16384 channels); larger sizes return VQLIN_ERR_UNSUPPORTED_SHAPE.
+ * It allocates nothing and calls no allocating routine.  Y equals what
+ * vqlin_linear_w4a4_static computes for the same arguments; the codes are not
+ * returned.
+ *
+ * - The first call on a device looks up the array's device address on that
+ *   device (cudaGetSymbolAddress); make that first call before any stream
+ *   capture that includes this entry point.
+ * - Every call on a device shares the array, and the array keeps the last
+ *   call's codes.  Nothing in it has to start at zero: each call writes every
+ *   code it reads.  Calls whose kernels overlap on the GPU (different streams
+ *   without ordering between them) race on the array and may compute wrong
+ *   results; order them, for example on one stream.
+ */
+vqlin_status vqlin_linear_w4a4_static_noalloc(const uint16_t* X, const float* static_scale,
+                                              int hadamard_block, const uint8_t* wq, const float* sw,
+                                              const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                              void* stream);
+
 /* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
  * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands;
  * float32 partial sums cover at most 1024 channels, which bounds them below
