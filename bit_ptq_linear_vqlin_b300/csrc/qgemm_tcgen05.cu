@@ -833,6 +833,11 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
       if (ns < ns_min) ns = ns_min;
       if (ns < 2) ns = 2;
       while (ns > ns_min && ns > 2 && smem_bytes(bt, ns, FX, RAW) > (size_t)kMaxSmem) --ns;
+      // A stage is reused by the k-block NS later, and the two expander groups
+      // take alternate k-blocks: with NS odd, a group would wait on a stage
+      // whose previous use belongs to the other group, where an mbarrier parity
+      // wait cannot tell a pending phase from the one before it
+      if (per_cta > ns && (ns & 1)) ns += ns - 1 >= ns_min && ns - 1 >= 2 ? -1 : 1;
       uint32_t c = 32;
       while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
       if (c > 512 || smem_bytes(bt, ns, FX, RAW) > (size_t)kMaxSmem) continue;

@@ -25,11 +25,18 @@
 //     weight tile (32 bytes of each row per 64-channel k-block);
 //   * warps 2..9: expand the packed weights into bf16 (q - z) directly in
 //     tensor memory (thread = weight row, tcgen05.st), the MMA's A operand;
-//   * warp 1: tensor memory and the MMAs (kind::f16, bf16 x bf16 -> f32, A
-//     from tensor memory), one accumulator per group, double-buffered;
-//   * warps 10..13: drain each group's accumulator, y += s[n,g] * partial, in
-//     registers; then the bias epilogue, with split K summed over the
-//     cluster's shared memory in a fixed order (deterministic).
+//   * MMAs (kind::f16, bf16 x bf16 -> f32, A from tensor memory) from up to
+//     four issuing warps (1, 14, 15, 16), issuer i taking every NI-th
+//     quantization group of the CTA into an accumulator of its own: one
+//     thread issues at most one tcgen05.mma per ~120 SM clocks on B300
+//     whatever N, and a bf16 MMA covers only 16 channels, so a single issuer
+//     bounded the kernel at a few tokens; an issuer reuses its accumulator
+//     once the previous group in it has been drained;
+//   * warps 10..13 and 17..20: drain each group's accumulator (in group
+//     order), y += s[n,g] * partial, in registers, two warps per lane quadrant
+//     with 32 tokens each, so that one tensor-memory round trip (~300 SM
+//     clocks) covers a group; then the bias epilogue, with split K summed
+//     over the cluster's shared memory in a fixed order (deterministic).
 // Every wait is bounded in time (VQLIN_ERR_TIMEOUT in the status word).
 #include <mutex>
 
@@ -45,9 +52,10 @@ constexpr int kKB = 64;           // channels per k-block (one 128-byte bf16 row
 constexpr int kRawRow = 32;       // packed weight bytes of one row per k-block
 constexpr int kBRow = 128;        // activation bytes of one row per k-block
 constexpr int kACols = 32;        // tensor-memory columns of one A stage
-constexpr int kThreads = 448;     // 14 warps
+constexpr int kThreads = 672;     // 21 warps
 constexpr int kExpandWarps = 8;
-constexpr int kDrainThreads = 128;
+constexpr int kDrainThreads = 256;  // 8 warps
+constexpr int kMaxIssuers = 4;
 constexpr int kMaxSplit = 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
@@ -61,6 +69,8 @@ struct W4a16Args {
   int stages;
   uint32_t tmem_cols;
   uint32_t a_col;          // first tensor-memory column of the A stages
+  uint32_t acc_step;       // tensor-memory columns between the issuers' accumulators
+  int issuers;             // MMA-issuing warps (1..4), one accumulator each
   int rows_per;            // split K: output channels each cluster rank owns
   uint64_t wait_limit_ns;
 };
@@ -109,9 +119,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   uint64_t* full = bars;              // TMA -> expanders
   uint64_t* aready = bars + NS;       // expanders -> MMA
   uint64_t* empty = bars + 2 * NS;    // MMA -> TMA
-  uint64_t* accf = bars + 3 * NS;     // [2] MMA -> drain
-  uint64_t* acce = accf + 2;          // [2] drain -> MMA
-  uint64_t* done = acce + 2;          // every MMA issued has completed
+  uint64_t* accf = bars + 3 * NS;     // [issuer] MMA -> drain (a group accumulated)
+  uint64_t* acce = accf + kMaxIssuers;  // [issuer] drain -> MMA (accumulator free)
+  uint64_t* done = acce + kMaxIssuers;  // every MMA issued has completed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z;
@@ -131,11 +141,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       mbar_init(&aready[i], kExpandWarps / 2);  // one group of four warps per k-block
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxIssuers; ++i) {
       mbar_init(&accf[i], 1);
       mbar_init(&acce[i], kDrainThreads / 32);
     }
-    mbar_init(done, 1);
+    mbar_init(done, a.issuers);
     mbar_init_fence();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -146,9 +156,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  float y[BT];
+  // drain warps: 32 tokens [32 half, 32 half + 32) of their lane quadrant
+  constexpr int kHalfCols = BT < 32 ? BT : 32;
+  const bool drain = (warp >= 10 && warp < 14) || warp >= 17;
+  const int half = warp >= 17 ? 1 : 0;
+  const int ncol = BT - 32 * half < kHalfCols ? BT - 32 * half : kHalfCols;  // <= 0: no tokens
+  float y[kHalfCols];
 #pragma unroll
-  for (int c = 0; c < BT; ++c) y[c] = 0.0f;
+  for (int c = 0; c < kHalfCols; ++c) y[c] = 0.0f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -189,29 +204,38 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
           record_timeout(a.status, abort);
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    // the whole warp runs the loop (every wait decided by a vote); one elected
-    // lane issues each MMA and commit
-    {
-      const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
-      // stage, phase and group advance incrementally (no divisions)
-      const uint64_t db0 = sdesc_sw128(base);
-      const uint32_t ta0 = tmem + a.a_col;
-      int s = 0, kin = 0, jl = 0;  // stage; k-block inside the group; local group
-      uint32_t ph = 0;             // phase parity of stage s
-      for (int i = 0; i < cnt; ++i) {
-        const uint32_t acc = tmem + (uint32_t)((jl & 1) * BT);
-        if (kin == 0 && jl >= 2) {
-          const bool ok = mbar_wait_bounded(&acce[jl & 1], ((jl >> 1) - 1) & 1, a.wait_limit_ns, abort);
-          if (!__all_sync(0xffffffffu, ok)) {
-            if (!ok && !*abort) record_timeout(a.status, abort);
-            break;
-          }
-        }
-        const bool ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+  } else if (warp == 1 || (warp >= 14 && warp - 13 < a.issuers)) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer i: local groups i, i + NI, ...; the whole warp runs the loop
+    // (every wait decided by a vote) and one elected lane issues each MMA and
+    // commit; ring stage and phase advance incrementally (no divisions in the
+    // issue loop)
+    const int NI = a.issuers;
+    const int iss = warp == 1 ? 0 : warp - 13;
+    const uint32_t id = idesc_f32acc(1u, kTileN, BT);  // bf16 x bf16 -> f32
+    const uint64_t db0 = sdesc_sw128(base);
+    const uint32_t ta0 = tmem + a.a_col;
+    const uint32_t acc = tmem + (uint32_t)iss * a.acc_step;
+    int s = (iss * KB_PER_G) % NS;                     // ring stage of this issuer's first k-block
+    uint32_t ph = (uint32_t)(((iss * KB_PER_G) / NS) & 1);
+    const int skip = (NI - 1) * KB_PER_G;              // k-blocks of the other issuers between two groups
+    bool ok = true;
+    int round = 0;
+    for (int jl = iss; jl < ng && ok; jl += NI, ++round) {
+      if (round > 0) {
+        // the previous group in this accumulator has been drained
+        ok = mbar_wait_bounded(&acce[iss], (uint32_t)((round - 1) & 1), a.wait_limit_ns, abort);
         if (!__all_sync(0xffffffffu, ok)) {
           if (!ok && !*abort) record_timeout(a.status, abort);
+          ok = false;
+          break;
+        }
+      }
+      for (int kin = 0; kin < KB_PER_G; ++kin) {
+        ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (!ok && !*abort) record_timeout(a.status, abort);
+          ok = false;
           break;
         }
         tc_fence_after();
@@ -222,18 +246,20 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         mma_f16_ta_warp(acc, ta + 16, db + 4, id, 1u);
         mma_f16_ta_warp(acc, ta + 24, db + 6, id, 1u);
         tc_commit_warp(&empty[s]);
-        if (++kin == KB_PER_G) {
-          tc_commit_warp(&accf[jl & 1]);
-          kin = 0;
-          ++jl;
-        }
         if (++s == NS) {
           s = 0;
           ph ^= 1u;
         }
       }
-      tc_commit_warp(done);  // tensor memory is freed only after this completes
+      if (!ok) break;
+      tc_commit_warp(&accf[iss]);
+      s += skip;
+      while (s >= NS) {
+        s -= NS;
+        ph ^= 1u;
+      }
     }
+    tc_commit_warp(done);  // tensor memory is freed only after every issuer's MMAs completed
   } else if (warp < 10) {
     // ------------------------------------------------- weight expanders (2..9)
     // thread = weight row; the two groups of four warps (one warp per lane
@@ -290,32 +316,39 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         zz_next = jl + jstep < ng ? zero_pair(a, n, g0 + jl + jstep) : 0u;
       }
     }
-  } else {
-    // ------------------------------------------------ group drains (10..13)
+  } else if (drain) {
+    // --------------------------------------- group drains (10..13, 17..20)
     const int q = warp & 3, row = q * 32 + lane, n = n0 + row;
     float sg_next = 0.0f;
     if (ng > 0 && n < a.N) sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0) << 16);
+    int iss = 0, round = 0;  // issuer of group jl and its round (no divisions)
     for (int jl = 0; jl < ng; ++jl) {
       const float sg = sg_next;
       if (jl + 1 < ng && n < a.N)
         sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0 + jl + 1) << 16);
-      const bool ok = mbar_wait_bounded(&accf[jl & 1], (jl >> 1) & 1, a.wait_limit_ns, abort);
+      const bool ok = mbar_wait_bounded(&accf[iss], (uint32_t)(round & 1), a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < BT; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((jl & 1) * BT + c0), v);
+      if (ncol > 0) {
+        // every load of the group first, then one wait
+        uint32_t v[2][16];
+        const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)iss * a.acc_step + (uint32_t)(32 * half);
+        tmem_ld_x16(src, v[0]);
+        if (kHalfCols > 16) tmem_ld_x16(src + 16, v[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) y[c0 + j] = fmaf(sg, __uint_as_float(v[j]), y[c0 + j]);
+        for (int j = 0; j < kHalfCols; ++j) y[j] = fmaf(sg, __uint_as_float(v[j >> 4][j & 15]), y[j]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[jl & 1]);
+      if (lane == 0) mbar_arrive(&acce[iss]);
+      if (++iss == a.issuers) {
+        iss = 0;
+        ++round;
+      }
     }
   }
 
@@ -323,13 +356,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   __syncwarp();
   pdl_wait();  // global writes only once the previous kernel has finished
   if (S == 1) {
-    if (warp >= 10 && !*abort) {
+    if (drain && !*abort && ncol > 0) {
       const int row = (warp & 3) * 32 + lane, n = n0 + row;
       if (n < a.N) {
         const float b = a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n) << 16) : 0.0f;
 #pragma unroll
-        for (int c = 0; c < BT; ++c)
-          if (m0 + c < a.M) a.Y[(size_t)(m0 + c) * a.N + n] = f32_to_bf16_rn(__fadd_rn(y[c], b));
+        for (int c = 0; c < kHalfCols; ++c) {
+          const int m = m0 + 32 * half + c;
+          if (c < ncol && m < a.M) a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(__fadd_rn(y[c], b));
+        }
       }
     }
     tc_fence_before();
@@ -338,10 +373,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // float partial tile part[token][channel] over the idle stages
     float* part = reinterpret_cast<float*>(base);
     __syncthreads();  // every role is past the stages before they are overwritten
-    if (warp >= 10 && !*abort) {
+    if (drain && !*abort && ncol > 0) {
       const int row = (warp & 3) * 32 + lane;
 #pragma unroll
-      for (int c = 0; c < BT; ++c) part[c * kTileN + row] = y[c];
+      for (int c = 0; c < kHalfCols; ++c)
+        if (c < ncol) part[(32 * half + c) * kTileN + row] = y[c];
     }
     tc_fence_before();
     cluster_sync_all();
@@ -403,19 +439,29 @@ constexpr size_t stage_bytes() {
 
 template <int BT>
 size_t smem_bytes(int stages) {
-  return 1024 + stages * stage_bytes<BT>() + (3 * stages + 5) * 8;
+  return 1024 + stages * stage_bytes<BT>() + (3 * stages + 2 * kMaxIssuers + 1) * 8;
 }
 
 template <int BT, int GROUP>
 vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z,
                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
+  // function attributes are per device: set them once for every device used
+  static std::mutex mu;
+  static bool set[64] = {};
+  static cudaError_t res[64] = {};
+  cudaError_t attr_err = cudaSuccess;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: no device");
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev]) {
+      res[dev] = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      if (res[dev] == cudaSuccess)
+        res[dev] = cudaFuncSetAttribute(w4a16_tc_kernel<BT, GROUP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      set[dev] = true;
+    }
+    attr_err = res[dev];
+  }
   if (attr_err != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + BT - 1) / BT;
@@ -423,20 +469,45 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
   s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
   s_want = s_want > G ? G : s_want;
-  // the largest split whose clusters are all resident at once (one wave)
-  int S = 0, NS = 0, rows_per = 0;
+  // Among the splits whose clusters are all resident at once (one wave), the
+  // one of least estimated time (figures measured on B300): the MMAs, ~120 SM
+  // clocks per instruction per issuing warp at 2 GHz, overlap the activation
+  // tiles streaming in at ~200 GB/s per SM; split K adds its reduction over
+  // shared memory between the CTAs of a cluster, ~30 GB/s per SM plus ~0.3 us.
+  // Without a one-wave split, the smallest split.
+  int S = 0, NS = 0, rows_per = 0, NI = 0;
+  bool have_wave = false;
+  double best = 0.0;
   uint32_t a_col = 0, cols = 0;
+  const uint32_t acc_step = (uint32_t)((BT + 31) / 32 * 32);
   size_t dyn = 0;
   for (int s_try = s_want; s_try >= 1; --s_try) {
     const int per_cta = (G + s_try - 1) / s_try * (GROUP / kKB);
-    // stages: up to 4, no more than the k-blocks a CTA runs, and enough that
+    // stages: up to 8, no more than the k-blocks a CTA runs, and enough that
     // the float partial tile of the split-K epilogue ([BT][128]) fits over them
     const int ns_min = (int)(((size_t)BT * kTileN * 4 + stage_bytes<BT>() - 1) / stage_bytes<BT>());
-    int ns = per_cta > 4 ? 4 : per_cta;
+    int ns = per_cta > 8 ? 8 : per_cta;
     if (ns < ns_min) ns = ns_min;
     if (ns < 2) ns = 2;
-    // tensor memory: two group accumulators [0, 2 BT), then one A slot per stage
-    const uint32_t ac = (uint32_t)((2 * BT + 31) / 32 * 32);
+    // issuers: up to four, no more than the groups a CTA sums
+    const int groups = (G + s_try - 1) / s_try;
+    int ni = groups < kMaxIssuers ? groups : kMaxIssuers;
+    if (ni < 1) ni = 1;
+    // tensor memory: one accumulator per issuer, then one A slot per stage
+    while (ni > 1 && (uint32_t)ni * acc_step + (uint32_t)(ns * kACols) > 512) --ni;
+    while (ns > ns_min && ns > 2 && (uint32_t)ni * acc_step + (uint32_t)(ns * kACols) > 512) --ns;
+    // A ring stage is reused by the k-block NS later.  mbarrier parity waits
+    // tell only adjacent phases apart, so the role that waits for a stage's
+    // next use must be the one that consumed its last use: the two expander
+    // groups take alternate k-blocks (NS even), and issuer i takes whole
+    // groups every NI groups (NS a multiple of NI x k-blocks per group; with
+    // issuer 2 of 3 starting in a stage's second phase while its first was
+    // still pending, a parity wait would pass at once).
+    if (per_cta > ns) {
+      if (ns & 1) ns += ns - 1 >= ns_min ? -1 : 1;  // the partial tile still fits
+      while (ni > 1 && ns % (ni * (GROUP / kKB)) != 0) --ni;
+    }
+    const uint32_t ac = (uint32_t)ni * acc_step;
     uint32_t c = 32;
     while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
     if (c > 512 || smem_bytes<BT>(ns) > (size_t)kMaxSmem) continue;
@@ -444,10 +515,21 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     size_t d = smem_bytes<BT>(ns);
     const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
     if (d < dyn_floor) d = dyn_floor;
-    S = s_try; NS = ns; a_col = ac; cols = c; dyn = d;
-    rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
     const int active = vqlin::max_active_clusters((const void*)w4a16_tc_kernel<BT, GROUP>, kThreads, d, s_try);
-    if (tiles_n * tiles_m <= active) break;
+    const bool wave = tiles_n * tiles_m <= active;
+    const double t_mma = per_cta * 4.0 * 120.0 / ni / 2000.0;
+    const double t_x = per_cta * (double)BT * kBRow / 200e3;
+    const double t_red = s_try > 1 ? 0.3 + (double)(s_try - 1) / s_try * BT * kTileN * 4 / 30e3 : 0.0;
+    const double est = (t_mma > t_x ? t_mma : t_x) + t_red;
+    const bool take = S == 0 || (wave && (!have_wave || est < best)) || (!wave && !have_wave && s_try < S);
+    if (take) {
+      S = s_try; NS = ns; a_col = ac; cols = c; dyn = d; NI = ni;
+      rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+      if (wave) {
+        have_wave = true;
+        best = est;
+      }
+    }
   }
   if (S == 0) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "w4a16: no tile plan for M=%d N=%d K=%d", M, N, K);
 
@@ -463,6 +545,7 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   W4a16Args a;
   a.scales = s; a.zeros = z; a.bias = bias; a.Y = Y; a.status = status;
   a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
+  a.acc_step = acc_step; a.issuers = NI;
   a.rows_per = rows_per; a.wait_limit_ns = kWaitLimitNs;
 
   cudaLaunchConfig_t cfg = {};
