@@ -22,7 +22,10 @@
 //     range of whole groups of K; the S CTAs that split K form a cluster;
 //   * warp 0: TMA producer; a stage holds the activation tile (bf16, written
 //     by TMA directly in the 128-byte-swizzled MMA layout) and the packed
-//     weight tile (32 bytes of each row per 64-channel k-block);
+//     weight tile (32 bytes of each row per 64-channel k-block), each with a
+//     barrier of its own: the weights of the first stages (and the CTA's zero
+//     points and scales) are read and expanded before the previous kernel is
+//     waited for, so in a chain of launches that work overlaps it;
 //   * warps 2..9: expand the packed weights into bf16 (q - z) directly in
 //     tensor memory (thread = weight row, tcgen05.st), the MMA's A operand;
 //   * MMAs (kind::f16, bf16 x bf16 -> f32, A from tensor memory) from up to
@@ -57,6 +60,7 @@ constexpr int kExpandWarps = 8;
 constexpr int kDrainThreads = 256;  // 8 warps
 constexpr int kMaxIssuers = 4;
 constexpr int kMaxSplit = 16;
+constexpr int kMaxGroupsCta = 128;  // quantization groups of one CTA (zero points and scales in shared memory)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct W4a16Args {
@@ -72,6 +76,7 @@ struct W4a16Args {
   uint32_t acc_step;       // tensor-memory columns between the issuers' accumulators
   int issuers;             // MMA-issuing warps (1..4), one accumulator each
   int rows_per;            // split K: output channels each cluster rank owns
+  int ng_max;              // quantization groups of the CTA with the most (<= kMaxGroupsCta)
   uint64_t wait_limit_ns;
 };
 
@@ -94,14 +99,6 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zz, uint32_t* 
   o[3] = bf16x2_sub(((w >> 12) & 0x000F000Fu) | 0x43004300u, zz);
 }
 
-// bf16x2 bit pattern of (128 + z, 128 + z) for the zero point of row n, group g.
-__device__ __forceinline__ uint32_t zero_pair(const W4a16Args& a, int n, int g) {
-  uint32_t z = 0;
-  if (n < a.N) z = (uint32_t)__uint_as_float((uint32_t)__ldg(a.zeros + (size_t)n * a.G + g) << 16);
-  const uint32_t h = 0x4300u + z;
-  return h | (h << 16);
-}
-
 template <int BT, int GROUP>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -116,12 +113,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int NS = a.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * kStageBytes);
-  uint64_t* full = bars;              // TMA -> expanders
+  uint64_t* full = bars;              // TMA -> expanders (packed weight tile)
   uint64_t* aready = bars + NS;       // expanders -> MMA
   uint64_t* empty = bars + 2 * NS;    // MMA -> TMA
-  uint64_t* accf = bars + 3 * NS;     // [issuer] MMA -> drain (a group accumulated)
+  uint64_t* fullx = bars + 3 * NS;    // TMA -> MMA (activation tile)
+  uint64_t* accf = bars + 4 * NS;     // [issuer] MMA -> drain (a group accumulated)
   uint64_t* acce = accf + kMaxIssuers;  // [issuer] drain -> MMA (accumulator free)
   uint64_t* done = acce + kMaxIssuers;  // every MMA issued has completed
+  // the CTA's zero points z (uint8) and scales (bf16 bits), [local group][row]
+  uint8_t* zsm = reinterpret_cast<uint8_t*>(done + 1);
+  uint16_t* ssm = reinterpret_cast<uint16_t*>(zsm + (size_t)a.ng_max * kTileN);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z;
@@ -138,6 +139,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
+      mbar_init(&fullx[i], 1);
       mbar_init(&aready[i], kExpandWarps / 2);  // one group of four warps per k-block
       mbar_init(&empty[i], 1);
     }
@@ -165,14 +167,33 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
   for (int c = 0; c < kHalfCols; ++c) y[c] = 0.0f;
 
+  // Zero points (expanders) and scales and bias (drains) of the CTA's rows
+  // and groups, read once before the previous kernel is waited for (weights
+  // do not depend on it): loaded one group at a time inside the loops, their
+  // global-memory latency stood between consecutive k-blocks.
+  float bias_r = 0.0f;
+  if (warp >= 2 && warp < 10) {
+    const int t = tid - 64, row = t & (kTileN - 1), n = n0 + row;
+    for (int g = t >> 7; g < ng; g += 2)
+      zsm[g * kTileN + row] =
+          n < a.N ? (uint8_t)__uint_as_float((uint32_t)__ldg(a.zeros + (size_t)n * a.G + g0 + g) << 16) : 0;
+    named_barrier(1, kExpandWarps * 32);
+  } else if (drain) {
+    const int row = (warp & 3) * 32 + lane, n = n0 + row;
+    for (int g = half; g < ng; g += 2) ssm[g * kTileN + row] = n < a.N ? __ldg(a.scales + (size_t)n * a.G + g0 + g) : 0;
+    if (S == 1 && a.bias != nullptr && n < a.N) bias_r = __uint_as_float((uint32_t)__ldg(a.bias + n) << 16);
+    named_barrier(2, kDrainThreads);
+  }
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = 0;
-      // weight tiles of the first stages before waiting for the previous kernel
+      // weight tiles of the first stages before waiting for the previous
+      // kernel: they are expanded into tensor memory while it still runs
       const int pre = cnt < NS ? cnt : NS;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], kStageBytes);
+        mbar_arrive_expect_tx(&full[i], kTileN * kRawRow);
         tma_load_2d(base + (size_t)i * kStageBytes + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[i]);
       }
       pdl_wait();
@@ -180,7 +201,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       // lets a chain of launches prefetch weights all at once
       pdl_trigger();
       for (int i = 0; i < pre; ++i) {
-        tma_load_2d(base + (size_t)i * kStageBytes, &tmX, (kb0 + i) * kKB, m0, &full[i]);
+        mbar_arrive_expect_tx(&fullx[i], kBBytes);
+        tma_load_2d(base + (size_t)i * kStageBytes, &tmX, (kb0 + i) * kKB, m0, &fullx[i]);
         ++issued;
       }
       int s = 0;        // stage of k-block i
@@ -191,9 +213,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           break;
         }
         uint8_t* st = base + (size_t)s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        mbar_arrive_expect_tx(&full[s], kTileN * kRawRow);
         tma_load_2d(st + kBBytes, &tmW, (kb0 + i) * kRawRow, n0, &full[s]);
-        tma_load_2d(st, &tmX, (kb0 + i) * kKB, m0, &full[s]);
+        mbar_arrive_expect_tx(&fullx[s], kBBytes);
+        tma_load_2d(st, &tmX, (kb0 + i) * kKB, m0, &fullx[s]);
         ++issued;
         if (++s == NS) {
           s = 0;
@@ -201,7 +224,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
       }
       for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
-        if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
+        if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr) ||
+            !mbar_wait_bounded(&fullx[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
           record_timeout(a.status, abort);
     }
   } else if (warp == 1 || (warp >= 14 && warp - 13 < a.issuers)) {
@@ -232,7 +256,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
       }
       for (int kin = 0; kin < KB_PER_G; ++kin) {
-        ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort);
+        ok = mbar_wait_bounded(&aready[s], ph, a.wait_limit_ns, abort) &&
+             mbar_wait_bounded(&fullx[s], ph, a.wait_limit_ns, abort);
         if (!__all_sync(0xffffffffu, ok)) {
           if (!ok && !*abort) record_timeout(a.status, abort);
           ok = false;
@@ -274,8 +299,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // jstep (one group per k-block: 2, else 1)
     constexpr int jstep = KB_PER_G == 1 ? 2 : 1;
     int jl = gr / KB_PER_G, kin = gr % KB_PER_G;
-    uint32_t zz = jl < ng ? zero_pair(a, n, g0 + jl) : 0u;
-    uint32_t zz_next = jl + jstep < ng ? zero_pair(a, n, g0 + jl + jstep) : 0u;
     int s = gr;        // stage of k-block i (NS >= 2)
     uint32_t ph = 0;   // phase parity of stage s
     for (int i = gr; i < cnt; i += 2) {
@@ -284,6 +307,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         if (!ok && !*abort) record_timeout(a.status, abort);
         break;
       }
+      const uint32_t zh = 0x4300u + zsm[jl * kTileN + row];  // bf16 128 + z
+      const uint32_t zz = zh | (zh << 16);
       const uint8_t* rawrow = base + (size_t)s * kStageBytes + kBBytes + row * kRawRow;
       const uint4 c0 = *reinterpret_cast<const uint4*>(rawrow + (sw << 4));
       const uint4 c1 = *reinterpret_cast<const uint4*>(rawrow + ((1 ^ sw) << 4));
@@ -312,20 +337,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       if (kin >= KB_PER_G) {  // this group's next k-block is in another quantization group
         kin -= KB_PER_G * (kin / KB_PER_G);
         jl += jstep;
-        zz = zz_next;
-        zz_next = jl + jstep < ng ? zero_pair(a, n, g0 + jl + jstep) : 0u;
       }
     }
   } else if (drain) {
     // --------------------------------------- group drains (10..13, 17..20)
-    const int q = warp & 3, row = q * 32 + lane, n = n0 + row;
-    float sg_next = 0.0f;
-    if (ng > 0 && n < a.N) sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0) << 16);
+    const int q = warp & 3, row = q * 32 + lane;
     int iss = 0, round = 0;  // issuer of group jl and its round (no divisions)
     for (int jl = 0; jl < ng; ++jl) {
-      const float sg = sg_next;
-      if (jl + 1 < ng && n < a.N)
-        sg_next = __uint_as_float((uint32_t)__ldg(a.scales + (size_t)n * a.G + g0 + jl + 1) << 16);
+      const float sg = __uint_as_float((uint32_t)ssm[jl * kTileN + row] << 16);
       const bool ok = mbar_wait_bounded(&accf[iss], (uint32_t)(round & 1), a.wait_limit_ns, abort);
       if (!__all_sync(0xffffffffu, ok)) {
         if (!ok && !*abort) record_timeout(a.status, abort);
@@ -359,11 +378,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     if (drain && !*abort && ncol > 0) {
       const int row = (warp & 3) * 32 + lane, n = n0 + row;
       if (n < a.N) {
-        const float b = a.bias != nullptr ? __uint_as_float((uint32_t)__ldg(a.bias + n) << 16) : 0.0f;
 #pragma unroll
         for (int c = 0; c < kHalfCols; ++c) {
           const int m = m0 + 32 * half + c;
-          if (c < ncol && m < a.M) a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(__fadd_rn(y[c], b));
+          if (c < ncol && m < a.M) a.Y[(size_t)m * a.N + n] = f32_to_bf16_rn(__fadd_rn(y[c], bias_r));
         }
       }
     }
@@ -438,8 +456,8 @@ constexpr size_t stage_bytes() {
 }
 
 template <int BT>
-size_t smem_bytes(int stages) {
-  return 1024 + stages * stage_bytes<BT>() + (3 * stages + 2 * kMaxIssuers + 1) * 8;
+size_t smem_bytes(int stages, int ng_max) {
+  return 1024 + stages * stage_bytes<BT>() + (4 * stages + 2 * kMaxIssuers + 1) * 8 + (size_t)ng_max * kTileN * 3;
 }
 
 template <int BT, int GROUP>
@@ -467,22 +485,31 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + BT - 1) / BT;
   const int G = K / GROUP;
   int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
-  s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
+  s_want = s_want > 8 ? 8 : s_want;  // beyond 8 the reduction over the cluster costs more than it saves
   s_want = s_want > G ? G : s_want;
+  // a CTA holds the zero points and scales of at most kMaxGroupsCta groups
+  const int s_min = (G + kMaxGroupsCta - 1) / kMaxGroupsCta;
+  if (s_min > kMaxSplit) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "w4a16: K=%d has too many groups", K);
+  if (s_want < s_min) s_want = s_min;
   // Among the splits whose clusters are all resident at once (one wave), the
-  // one of least estimated time (figures measured on B300): the MMAs, ~120 SM
-  // clocks per instruction per issuing warp at 2 GHz, overlap the activation
-  // tiles streaming in at ~200 GB/s per SM; split K adds its reduction over
-  // shared memory between the CTAs of a cluster, ~30 GB/s per SM plus ~0.3 us.
-  // Without a one-wave split, the smallest split.
+  // one of least estimated time, a fit to launches timed on B300 at 16 to 64
+  // tokens: ~1.9 us fixed, ~0.27 us per k-block of a CTA (its expansion into
+  // tensor memory paces the pipeline), ~1 us + 0.2 us per CTA for the
+  // reduction over the cluster's shared memory when K is split, and ~0.02 us
+  // per CTA.  Splits other than powers of two (clusters of 3 or 6 CTAs timed
+  // twice as slow) are left out unless the groups force one.  Without a
+  // one-wave split, the smallest split.
   int S = 0, NS = 0, rows_per = 0, NI = 0;
   bool have_wave = false;
   double best = 0.0;
   uint32_t a_col = 0, cols = 0;
   const uint32_t acc_step = (uint32_t)((BT + 31) / 32 * 32);
   size_t dyn = 0;
-  for (int s_try = s_want; s_try >= 1; --s_try) {
-    const int per_cta = (G + s_try - 1) / s_try * (GROUP / kKB);
+  int ng_max = 0;
+  for (int s_try = s_want; s_try >= s_min; --s_try) {
+    if ((s_try & (s_try - 1)) != 0 && s_try != s_min) continue;
+    const int groups = (G + s_try - 1) / s_try;  // of the CTA with the most
+    const int per_cta = groups * (GROUP / kKB);
     // stages: up to 8, no more than the k-blocks a CTA runs, and enough that
     // the float partial tile of the split-K epilogue ([BT][128]) fits over them
     const int ns_min = (int)(((size_t)BT * kTileN * 4 + stage_bytes<BT>() - 1) / stage_bytes<BT>());
@@ -490,7 +517,6 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     if (ns < ns_min) ns = ns_min;
     if (ns < 2) ns = 2;
     // issuers: up to four, no more than the groups a CTA sums
-    const int groups = (G + s_try - 1) / s_try;
     int ni = groups < kMaxIssuers ? groups : kMaxIssuers;
     if (ni < 1) ni = 1;
     // tensor memory: one accumulator per issuer, then one A slot per stage
@@ -510,20 +536,18 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     const uint32_t ac = (uint32_t)ni * acc_step;
     uint32_t c = 32;
     while (c < ac + (uint32_t)(ns * kACols)) c <<= 1;
-    if (c > 512 || smem_bytes<BT>(ns) > (size_t)kMaxSmem) continue;
+    if (c > 512 || smem_bytes<BT>(ns, groups) > (size_t)kMaxSmem) continue;
     // never more CTAs on an SM than its tensor memory holds (see the integer GEMM)
-    size_t d = smem_bytes<BT>(ns);
+    size_t d = smem_bytes<BT>(ns, groups);
     const size_t dyn_floor = kSmemPerSm / (512 / c + 1) + 1;
     if (d < dyn_floor) d = dyn_floor;
     const int active = vqlin::max_active_clusters((const void*)w4a16_tc_kernel<BT, GROUP>, kThreads, d, s_try);
     const bool wave = tiles_n * tiles_m <= active;
-    const double t_mma = per_cta * 4.0 * 120.0 / ni / 2000.0;
-    const double t_x = per_cta * (double)BT * kBRow / 200e3;
-    const double t_red = s_try > 1 ? 0.3 + (double)(s_try - 1) / s_try * BT * kTileN * 4 / 30e3 : 0.0;
-    const double est = (t_mma > t_x ? t_mma : t_x) + t_red;
+    const int ctas = tiles_n * tiles_m * s_try;
+    const double est = 1.9 + 0.27 * per_cta + (s_try > 1 ? 1.0 + 0.2 * s_try : 0.0) + 0.02 * ctas;
     const bool take = S == 0 || (wave && (!have_wave || est < best)) || (!wave && !have_wave && s_try < S);
     if (take) {
-      S = s_try; NS = ns; a_col = ac; cols = c; dyn = d; NI = ni;
+      S = s_try; NS = ns; a_col = ac; cols = c; dyn = d; NI = ni; ng_max = groups;
       rows_per = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
       if (wave) {
         have_wave = true;
@@ -546,7 +570,7 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   a.scales = s; a.zeros = z; a.bias = bias; a.Y = Y; a.status = status;
   a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
   a.acc_step = acc_step; a.issuers = NI;
-  a.rows_per = rows_per; a.wait_limit_ns = kWaitLimitNs;
+  a.rows_per = rows_per; a.ng_max = ng_max; a.wait_limit_ns = kWaitLimitNs;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, S);
