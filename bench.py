@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-sample-rows", type=int, default=64,
                     help="prefix tokens per projection in the CPU-oracle sample")
+    ap.add_argument("--skip-shapes", action="store_true",
+                    help="leave out the per-shape lines (configs 1-4) after the control step")
     ap.add_argument("--shape", default=None,
                     help="time one kernel class alone instead of the control step: KIND,M,N,K with KIND in "
                          "act_quant4, act_quant8, act_quant_static4, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a8, "
@@ -184,6 +186,60 @@ def oracle_run(prep):
     return per_step, sample, t3 - t0
 
 
+def oracle_single_thread(seed: int, rows: int):
+    """The same oracle sample on one host thread: a child process whose BLAS
+    pools are limited to one thread before numpy loads (no GPU use)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "p = bench.oracle_prepare(%d, %d); r = bench.oracle_run(p); "
+            "print(json.dumps({'per_step': r[0], 'sample_s': r[2], 'threads': bench.blas_threads()}))"
+            % (ROOT, seed, rows))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        d = json.loads(out.stdout.strip().splitlines()[-1])
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        return None
+    return {"value": 1.0 / d["per_step"], "unit": UNIT, "cores": d["threads"], "sample_s": d["sample_s"]}
+
+
+def oracle_tie_fraction(prep, vq, torch, dev):
+    """Activation codes of the GPU kernel against the oracle's on the sample's
+    inputs: the fraction that differ, and whether every difference sits within
+    1e-4 of a rounding tie of the exactly rotated value (the only place the two
+    may differ: the kernel rotates in float32, the oracle in float64)."""
+    import numpy as np
+
+    from oracle import vqlin_oracle as o
+    from synth import workloads as wl
+
+    hb = wl.WORKLOADS["prefix_w4a4_w8a8"]["hadamard_block"]
+    total = bad_n = 0
+    all_at_ties = True
+    cases = [(X, bits, None) for X, bits, _ in prep["pre_groups"]]
+    cases += [(X, 4, s_static) for X, _, _, s_static in prep["exp_groups"]]
+    for X, bits, st in cases:
+        q_ref, s_ref = o.act_hadamard_quant(X, bits, hb, st)
+        Xd = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).to(dev).view(torch.bfloat16)
+        std = None if st is None else torch.tensor([st], dtype=torch.float32, device=dev)
+        q, _ = vq.act_hadamard_quant(Xd, bits, hb, static_scale=std)
+        qn = q.cpu().numpy()
+        q_gpu = o.decode_act_int4(qn) if bits == 4 else o.decode_act_int8(qn.view(np.uint16))
+        diff = np.nonzero(q_gpu.astype(np.int64) - q_ref.astype(np.int64))
+        if diff[0].size:
+            safe = np.where(s_ref > 0, s_ref, 1).astype(np.float64)
+            exact = o.rotated_f64(X, hb) / (safe[:, None] if np.ndim(safe) else safe)
+            frac = np.abs(exact[diff] - np.floor(exact[diff]) - 0.5)
+            all_at_ties = all_at_ties and bool(np.all(frac < 1e-4))
+        total += q_ref.size
+        bad_n += diff[0].size
+    return {"fraction": bad_n / max(total, 1), "codes_compared": total, "mismatches": bad_n,
+            "all_within_1e-4_of_a_tie": all_at_ties,
+            "inputs": "the CPU sample's activations: prefix (4 inputs, dynamic scales) and expert (static scales)"}
+
+
 def blas_threads() -> int:
     try:
         import threadpoolctl
@@ -201,22 +257,29 @@ def run_reference(args):
         return 0  # the CPU oracle arm runs on rank 0 only
     import numpy as np  # noqa: F401  (loads BLAS so its thread count is visible)
 
-    times = []
+    times, samples = [], []
     sample_desc = ""
     prep = oracle_prepare(args.seed, args.cpu_sample_rows)
+    t_region = 0.0
     for i in range(args.warmup + args.steps):
-        per_step, sample_desc, _ = oracle_run(prep)
+        t0 = time.perf_counter()
+        per_step, sample_desc, sample_s = oracle_run(prep)
         if i >= args.warmup:
+            t_region += time.perf_counter() - t0
             times.append(per_step)
+            samples.append(sample_s)
     sec = sum(times) / len(times)
     value = 1.0 / sec
     cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_region / args.steps * 1e3,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (numpy oracle)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "timing": "host wall clock of the oracle on a bounded sample, "
-                   "extrapolated to one control step"},
+        "config": {"workload": WORKLOAD, "timing": "host wall clock of the oracle: each step is one bounded "
+                   "sample (ms_per_step is its real time); value extrapolates the sample to whole control "
+                   "steps by tokens and layers",
+                   "extrapolated_ms_per_control_step": sec * 1e3},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -376,23 +439,14 @@ class ControlStepStack:
 
     # -- algorithmic work ------------------------------------------------------
     def work_of(self, key):
-        """(flops, bytes) of one launch of a kernel class (formulas of the scope table)."""
+        """(flops, bytes) of one launch of a kernel class, bytes by the scope
+        table's formulas (int4 codes half a byte, int8 codes one byte)."""
         kind = key[0]
         if kind.startswith("act_quant"):
             bits, M, K = key[1], key[2], key[3]
-            return 0, 2 * M * K + M * K * (1 if bits == 4 else 2) + 4 * M
+            return 0, alg_bytes(f"act_quant{bits}", M, 0, K)
         M, N, K = key[1], key[2], key[3]
-        if kind == "linear_w4a4":
-            return 2 * M * N * K, M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
-        if kind == "linear_w4a4_static":  # bf16 activations in, one scale
-            return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 + 4 * N + 2 * M * N
-        if kind == "linear_w8a8":
-            return 2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N
-        if kind == "linear_w4a8":
-            return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
-        if kind == "linear_w4a16":
-            return 2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // self.group + 2 * M * N
-        raise KeyError(key)
+        return 2 * M * N * K, alg_bytes(kind, M, N, K, self.group)
 
 
 def capture(torch, fn):
@@ -633,35 +687,41 @@ def run_vqlin(args):
     h2d = h_pre.numel() * 2 + h_exp.numel() * 2
     d2h = h_out4.numel() * 2 + h_out16.numel() * 2
 
-    # -- roofline of the dominant kernel class
+    # -- tensor-core peaks: the library's own rate kernels for the MMA kinds used
     peaks, peaks_src = load_peaks()
+    own = measure_tensor_peaks(stack.vq)
+
+    # -- roofline of the dominant kernel class
     flops, nbytes = stack.work_of(dom)
-    if dom[0].startswith("act_quant") or dom[0] == "linear_w4a16" or dom[1] <= 64:
+    kind_peak = "e4m3" if dom[0] in ("linear_w4a4", "linear_w4a4_static") else "bf16"
+    rl = roofline_of(flops, nbytes, dom_avg_ms * 1e3, own[kind_peak]["tflops"], peaks["hbm_gbs"])
+    if rl["bound"] == "hbm":
         bound, achieved, peak, unit = "hbm", nbytes / (dom_avg_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
-        peak_note = f"hbm_gbs ({peaks_src})"
-    elif dom[0] in ("linear_w4a4", "linear_w4a4_static"):
-        bound, unit = "tensor", "TFLOP/s"
-        achieved = flops / (dom_avg_ms / 1e3) / 1e12
-        peak = 2.0 * peaks["bf16_tflops"]
-        peak_note = (f"dense fp8 rate = 2 x bf16_tflops ({peaks_src}, burst: the class is timed alone); the "
-                     "int4 codes run on kind::f8f6f4 (e4m3) MMAs")
+        peak_note = f"hbm_gbs of MEASURED_PEAKS.json ({peaks_src}, a STREAM-style copy)"
     else:
         bound, unit = "tensor", "TFLOP/s"
         achieved = flops / (dom_avg_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        peak_note = (f"dense f16 rate = bf16_tflops ({peaks_src}, burst: the class is timed alone); the int8 "
-                     "codes run on kind::f16 MMAs")
+        peak = own[kind_peak]["tflops"]
+        peak_note = (f"the library's own dense tcgen05 rate for the MMA kind this kernel issues "
+                     f"({'kind::f8f6f4 e4m3' if kind_peak == 'e4m3' else 'kind::f16 bf16'}), measured in this run")
     traffic = read_traffic(dom)
 
-    # -- CPU oracle baseline (rank 0 only)
+    # -- per-shape lines of configs 1-4 (rank 0)
+    shapes = None
+    if rank == 0 and not args.skip_shapes:
+        shapes = per_shape_lines(torch, stack.vq, dev, args.seed, own, peaks["hbm_gbs"])
+
+    # -- CPU oracle baseline (rank 0 only): all cores and one thread
     cpu = None
     if rank == 0:
         prep = oracle_prepare(args.seed, args.cpu_sample_rows)
         runs = [oracle_run(prep) for _ in range(3)]
         per_step = sum(r[0] for r in runs) / len(runs)
         sample, sample_s = runs[0][1], sum(r[2] for r in runs)
+        single = oracle_single_thread(args.seed, args.cpu_sample_rows)
         cpu = {"value": 1.0 / per_step, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": sample + f" ({sample_s:.1f} s of host time)"}
+               "sample": sample + f" ({sample_s:.1f} s of host time over 3 runs)", "single_thread": single,
+               "activation_tie_fraction": oracle_tie_fraction(prep, stack.vq, torch, dev)}
 
     if rank == 0:
         line = {
@@ -669,11 +729,15 @@ def run_vqlin(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "s4/s8 codes (int32-exact sums) + bf16 x u4 (f32 accumulate)",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "inputs larger than L2: each step streams "
-                       f"{stack_bytes(stack) / 1e9:.2f} GB of distinct weights", "graphs": "CUDA graphs per part",
-                       "parallelism": f"replicas x{world}"},
+            "config": {"workload": WORKLOAD, "l2": "inputs larger than L2: "
+                       f"{stack_bytes(stack)[0] / 1e9:.2f} GB of distinct quantized weights (prefix 18 layers, "
+                       "expert 18 layers at W4A4 and W4A16); each step reads "
+                       f"{stack_bytes(stack)[1] / 1e9:.2f} GB of them, the expert's layers once per denoising "
+                       "step (their 0.15 GB per precision does not stay in the 126 MB L2)",
+                       "graphs": "CUDA graphs per part", "parallelism": f"replicas x{world}"},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": traffic,
+                         "bytes_formula": "scope table: int4 codes MK/2, int8 codes MK",
                          "kernel": " ".join(str(k) for k in dom), "avg_launch_ms": dom_avg_ms,
                          "launches_timed": dom_launches, "peak_source": peak_note,
                          "timing": "CUDA events around a graph of every launch of the class in one step "
@@ -690,6 +754,13 @@ def run_vqlin(args):
             "kernel_us_per_launch": {" ".join(str(x) for x in k): round(v[2] * 1e3, 2)
                                      for k, v in sorted(per_class.items(), key=lambda kv: -kv[1][0])},
             "wall_s_timed": t_wall,
+            "peaks": {"hbm_gbs": peaks["hbm_gbs"], "cublas_bf16_tflops": peaks["bf16_tflops"],
+                      "source": peaks_src, "tcgen05_e4m3_tflops": own["e4m3"]["tflops"],
+                      "tcgen05_bf16_tflops": own["bf16"]["tflops"], "tcgen05_how": own["bf16"]["how"],
+                      "int8_note": "kind::i8 does not assemble for sm_103a: int4 codes run exactly on "
+                                   "kind::f8f6f4 (e4m3), int8 codes on kind::f16; those rates are the "
+                                   "int-class peaks used"},
+            "per_shape": shapes,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -698,14 +769,268 @@ def run_vqlin(args):
 
 
 def stack_bytes(stack):
-    total = 0
+    """(distinct quantized weight bytes, weight bytes one control step reads):
+    the 18 expert layers are shared by the 10 denoising steps, read once per
+    step each."""
+    pre = exp = 0
     for layer in stack.pre_w:
         for w in layer:
-            total += w["q"].numel() * w["q"].element_size() + w["s"].numel() * 4
+            pre += w["q"].numel() * w["q"].element_size() + w["s"].numel() * 4
     for layer in stack.exp_w:
         for w in layer:
-            total += stack.n_steps * (w["q4"].numel() + w["q16"].numel() + 2 * w["s16"].numel() * 2)
-    return total
+            exp += (w["q4"].numel() + w["s4"].numel() * 4 + w["q16"].numel() + 2 * w["s16"].numel() * 2)
+    return pre + exp, pre + stack.n_steps * exp
+
+
+# ----------------------------------------------------------------------------- per-shape lines
+
+# Algorithmic bytes of one call (the scope table's formulas): int4 codes count
+# half a byte each and int8 codes one byte, whatever the storage format.
+def alg_bytes(kind, M, N, K, group=128):
+    if kind == "act_quant4":
+        return 2 * M * K + M * K // 2 + 4 * M
+    if kind == "act_quant8":
+        return 2 * M * K + M * K + 4 * M
+    if kind == "linear_w4a4":
+        return M * K // 2 + N * K // 2 + 4 * M + 4 * N + 2 * M * N
+    if kind == "linear_w8a8":
+        return M * K + N * K + 4 * M + 4 * N + 2 * M * N
+    if kind == "linear_w4a8":
+        return M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
+    if kind == "linear_w4a4_static":  # bf16 activations in, one static scale
+        return 2 * M * K + N * K // 2 + 4 + 4 * N + 2 * M * N
+    if kind == "linear_w4a16":
+        return 2 * M * K + N * K // 2 + 4 * N * K // group + 2 * M * N
+    if kind == "linear_bf16":
+        return 2 * M * K + 2 * N * K + 2 * M * N
+    raise KeyError(kind)
+
+
+# Bytes the library actually moves where its storage format differs: one byte
+# per int4 activation code, a 16-bit word per int8 code.
+def storage_bytes(kind, M, N, K, group=128):
+    if kind == "act_quant4":
+        return 2 * M * K + M * K + 4 * M
+    if kind == "act_quant8":
+        return 2 * M * K + 2 * M * K + 4 * M
+    if kind == "linear_w4a4":
+        return M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N
+    if kind in ("linear_w8a8", "linear_w4a8"):
+        return 2 * M * K + (N * K if kind == "linear_w8a8" else N * K // 2) + 4 * M + 4 * N + 2 * M * N
+    return alg_bytes(kind, M, N, K, group)
+
+
+def roofline_of(flops, nbytes, us, tensor_peak_tflops, hbm_gbs):
+    """Achieved rate against min(tensor peak, arithmetic intensity x HBM bandwidth)."""
+    if us <= 0:
+        return None
+    gbs = nbytes / us / 1e3
+    if not flops:
+        return {"bound": "hbm", "frac": gbs / hbm_gbs}
+    tops = flops / us / 1e6
+    ridge = flops / nbytes * hbm_gbs / 1e3  # TFLOP/s the HBM roofline allows
+    bound = "hbm" if ridge < tensor_peak_tflops else "tensor"
+    return {"bound": bound, "frac": tops / min(ridge, tensor_peak_tflops)}
+
+
+class ShapeTimer:
+    """Times launch sequences of one shape: every launch reads its own weight
+    copy (the copies together exceed 2x L2), captured in one CUDA graph and
+    timed with CUDA events on the launching stream."""
+
+    def __init__(self, torch, dev):
+        self.torch, self.dev = torch, dev
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def copies_for(self, weight_bytes):
+        return max(2, min(48, -(-2 * self.l2 // max(weight_bytes, 1))))
+
+    def time(self, fns, reps=8):
+        torch = self.torch
+
+        def body():
+            for f in fns:
+                f()
+        g = capture(torch, body)
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) * 1e3 / (reps * len(fns))
+
+
+def per_shape_lines(torch, vq, dev, seed, tensor_peaks, hbm_gbs):
+    """Per-shape lines of configs 1-4 (and the static-scale expert of config 5):
+    µs, TOPS, GB/s and roofline fraction of each quantized projection (its
+    activation quantization and GEMM also alone), next to cuBLAS bf16 on the
+    same shape in the same process."""
+    from synth import device as sd, workloads as wl
+
+    T = ShapeTimer(torch, dev)
+    lines = []
+    c1, c2, c3, c4 = (wl.WORKLOADS[k] for k in ("single_w4a4_16x256", "expert_w4a16", "prefix_w4a4_w8a8",
+                                                   "llama2_7b"))
+
+    def wgen(N, K, std, tags, spike=(0.0, 1.0)):
+        return sd.weights(N, K, std=std, spike_frac=spike[0], spike_scale=spike[1], seed=seed, tags=tags, device=dev)
+
+    def entry(cfg, variant, M, N, K, parts, hb, note=None):
+        """parts: list of (kind, us) making up the projection."""
+        us = sum(u for _, u in parts)
+        flops = 2 * M * N * K
+        nbytes = sum(alg_bytes(k, M, N, K) for k, _ in parts)
+        sbytes = sum(storage_bytes(k, M, N, K) for k, _ in parts)
+        tp = tensor_peaks["e4m3" if variant in ("w4a4", "w4a4_static") else "bf16"]
+        e = {"cfg": cfg, "variant": variant, "M": M, "N": N, "K": K, "hadamard_block": hb, "us": round(us, 3),
+             "TOPS": round(flops / us / 1e6, 2), "GBs": round(nbytes / us / 1e3, 1),
+             "alg_bytes": nbytes, "storage_bytes": sbytes,
+             "roofline": roofline_of(flops, nbytes, us, tp["tflops"], hbm_gbs)}
+        if len(parts) > 1:
+            e["parts"] = {}
+            for k, u in parts:
+                fl = 0 if k.startswith("act_quant") else flops
+                e["parts"][k] = {"us": round(u, 3),
+                                 "GBs": round(alg_bytes(k, M, N, K) / u / 1e3, 1),
+                                 "roofline": roofline_of(fl, alg_bytes(k, M, N, K), u, tp["tflops"], hbm_gbs)}
+        if note:
+            e["note"] = note
+        return e
+
+    def bf16_us(M, N, K, X, std, tags):
+        Ws = [wgen(N, K, std, tags + ("bf16", i)) for i in range(T.copies_for(2 * N * K))]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        us = T.time([lambda W=W: vq.linear_bf16_ref(X, W, out=y) for W in Ws])
+        del Ws
+        return us
+
+    def quant_us(X, bits, hb, M, K):
+        q = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=dev)
+        sx = torch.empty(M, device=dev)
+        us = T.time([lambda: vq.act_hadamard_quant(X, bits, hb, q_out=q, scale_out=sx)] * 16)
+        return us, q, sx
+
+    def int_variant(variant, X, M, N, K, hb, std, tags, cublas):
+        abits, wbits = {"w4a4": (4, 4), "w8a8": (8, 8), "w4a8": (8, 4)}[variant]
+        qus, xq, sx = quant_us(X, abits, hb, M, K)
+        n = T.copies_for(N * K // (2 if wbits == 4 else 1))
+        ws = []
+        for i in range(n):
+            q, s_ = vq.quantize_weights_rtn(wgen(N, K, std, tags + (i,)), wbits, True, 0, hb)
+            ws.append((q, s_))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = {"w4a4": vq.linear_w4a4, "w8a8": vq.linear_w8a8, "w4a8": vq.linear_w4a8}[variant]
+        gus = T.time([lambda q=q, s_=s_: fn(xq, sx, q, s_, out=y) for q, s_ in ws])
+        # the projection as a user runs it: quantize, then the GEMM, per weight copy
+        pus = T.time([lambda q=q, s_=s_: (vq.act_hadamard_quant(X, abits, hb, q_out=xq, scale_out=sx),
+                                          fn(xq, sx, q, s_, out=y)) for q, s_ in ws])
+        del ws
+        kq = f"act_quant{abits}"
+        e = entry(cfg_now[0], variant, M, N, K, [(kq, qus), (f"linear_{variant}", gus)], hb)
+        e["projection_us"] = round(pus, 3)
+        e["cublas_bf16_us"] = round(cublas, 3)
+        e["speedup_vs_bf16"] = round(cublas / pus, 3)
+        return e
+
+    def w4a16_variant(X, M, N, K, std, tags, cublas, spike=(0.0, 1.0), group=128):
+        n = T.copies_for(N * K // 2)
+        ws = [vq.quantize_weights_rtn(wgen(N, K, std, tags + ("w16", i), spike), 4, False, group, 0) for i in range(n)]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        us = T.time([lambda w=w: vq.linear_w4a16(X, w[0], w[1], w[2], group, out=y) for w in ws])
+        del ws
+        e = entry(cfg_now[0], "w4a16", M, N, K, [("linear_w4a16", us)], 0)
+        e["projection_us"] = round(us, 3)
+        e["cublas_bf16_us"] = round(cublas, 3)
+        e["speedup_vs_bf16"] = round(cublas / us, 3)
+        return e
+
+    def static_variant(X, M, N, K, hb, std, tags, cublas, spike):
+        n = T.copies_for(N * K // 2)
+        ws = [vq.quantize_weights_rtn(wgen(N, K, std, tags + ("w4s", i), spike), 4, True, 0, hb) for i in range(n)]
+        _, sc = vq.act_hadamard_quant(X, 4, hb)
+        st = sc.max().reshape(1).contiguous()
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        us = T.time([lambda w=w: vq.linear_w4a4_static(X, st, w[0], w[1], hb, out=y, xq_out=xq) for w in ws])
+        del ws
+        e = entry("5", "w4a4_static", M, N, K, [("linear_w4a4_static", us)], hb,
+                  note="one launch: rotation, static-scale quantization and GEMM")
+        e["projection_us"] = round(us, 3)
+        e["cublas_bf16_us"] = round(cublas, 3)
+        e["speedup_vs_bf16"] = round(cublas / us, 3)
+        return e
+
+    cfg_now = ["1"]
+    # ---- config 1: one W4A4 linear, 16 x 256 -> 256, block Hadamard 64
+    M, N, K = c1["M"], c1["N"], c1["K"]
+    X = sd.activations(M, K, n_outliers=c1["n_outliers"], outlier_scale=c1["outlier_scale"], seed=seed,
+                       tags=("shape1",), device=dev)
+    cb = bf16_us(M, N, K, X, c1["w_std"], ("shape1",))
+    e = int_variant("w4a4", X, M, N, K, c1["hadamard_block"], c1["w_std"], ("shape1",), cb)
+    e["roofline"]["bound"] = "latency"
+    e["note"] = "2.1 MOP and ~55 KB: launch latency bounds it, the fraction is not a target"
+    lines.append(e)
+
+    # ---- config 2 (W4A16) and the static-scale W4A4 expert of config 5, 50 tokens
+    cfg_now[0] = "2"
+    spike = (c2["spike_frac"], c2["spike_scale"])
+    for name, N, K in (("q|k|v", 3072, 1024), ("o", 1024, 1024), ("gate|up", 8192, 1024), ("down", 1024, 4096)):
+        M = c2["M"]
+        X = sd.activations(M, K, seed=seed, tags=("shape2", name), device=dev)
+        cb = bf16_us(M, N, K, X, c2["w_std"], ("shape2", name))
+        e = w4a16_variant(X, M, N, K, c2["w_std"], ("shape2", name), cb, spike, c2["group_size"])
+        e["projection"] = name
+        lines.append(e)
+        e = static_variant(X, M, N, K, 128, c2["w_std"], ("shape2", name), cb, spike)
+        e["projection"] = name
+        lines.append(e)
+
+    # ---- config 3: prefix backbone, 816 tokens
+    cfg_now[0] = "3"
+    for name, N, K, variant in (("q|k|v", 2560, 2048, "w4a4"), ("o", 2048, 2048, "w8a8"),
+                                ("gate|up", 32768, 2048, "w4a4"), ("down", 2048, 16384, "w8a8")):
+        M = c3["M"]
+        X = sd.activations(M, K, dist=c3["act_dist"], n_outliers=wl.n_outliers(K, c3["outlier_frac"]),
+                           outlier_scale=c3["outlier_scale"], seed=seed, tags=("shape3", name), device=dev)
+        cb = bf16_us(M, N, K, X, c3["w_std"], ("shape3", name))
+        e = int_variant(variant, X, M, N, K, c3["hadamard_block"], c3["w_std"], ("shape3", name), cb)
+        e["projection"] = name
+        lines.append(e)
+
+    # ---- config 4: Llama-2-7B-shaped projections at M in {1, 64, 512}
+    cfg_now[0] = "4"
+    for M in c4["Ms"]:
+        for name, N, K in (("q/k/v/o", 4096, 4096), ("gate/up", 11008, 4096), ("down", 4096, 11008)):
+            X = sd.activations(M, K, n_outliers=wl.n_outliers(K, c4["outlier_frac"]),
+                               outlier_scale=c4["outlier_scale"], seed=seed, tags=("shape4", M, name), device=dev)
+            cb = bf16_us(M, N, K, X, c4["w_std"], ("shape4", M, name))
+            for variant in ("w8a8", "w4a4", "w4a8"):
+                e = int_variant(variant, X, M, N, K, c4["hadamard_block"], c4["w_std"], ("shape4", M, name), cb)
+                e["projection"] = name
+                lines.append(e)
+            e = w4a16_variant(X, M, N, K, c4["w_std"], ("shape4", M, name), cb, group=c4["group_size"])
+            e["projection"] = name
+            lines.append(e)
+            torch.cuda.empty_cache()
+    return lines
+
+
+def measure_tensor_peaks(vq):
+    """The library's own dense tcgen05 rate for the two MMA kinds the GEMMs
+    issue: 148 CTAs, N = 256, four issuing warps with an accumulator each."""
+    out = {}
+    for kind in ("e4m3", "bf16"):
+        best = 0.0
+        for _ in range(3):
+            tf, _ = vq.measure_mma_rate(kind, 256, a_in_tmem=False, accumulators=1, issuers=1, iters=8192)
+            tf4, _ = vq.measure_mma_rate(kind, 64, a_in_tmem=False, accumulators=4, issuers=4, iters=8192)
+            best = max(best, tf, tf4)
+        out[kind] = {"tflops": best, "how": "vqlin_measure_mma_rate: one CTA per SM, operands on chip, "
+                     "best of one issuer at N=256 and four issuers at N=64, 3 tries"}
+    return out
 
 
 def run_shape(args):
@@ -792,6 +1117,8 @@ def run_shape(args):
     else:
         raise SystemExit(f"unknown kernel class {kind}")
 
+    # algorithmic bytes of the scope table (int4 codes MK/2, int8 codes MK)
+    nbytes = alg_bytes(("act_quant" + kind[-1]) if kind.startswith("act_quant") else kind, M, N, K, group)
     copies = max(2, min(64, -(-2 * l2 // max(per, 1))))
     data = [mk() for _ in range(copies)]
 

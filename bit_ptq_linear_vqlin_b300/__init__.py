@@ -29,7 +29,7 @@ __all__ = [
     "VqlinError", "load", "LIB_PATH",
     "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w4a4_static", "linear_w8a8",
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
-    "debug_gemm_withheld_loads", "measure_mma_rate",
+    "debug_gemm_withheld_loads", "debug_w4a16_withheld_loads", "measure_mma_rate",
     "get_last_device_error",
 ]
 
@@ -237,6 +237,22 @@ def debug_gemm_withheld_loads(bits: int, xq, wq, K: int, limit_ns: int, out=None
     check(_lib.vqlin_debug_gemm_withheld_loads(bits, _ptr(xq), _ptr(wq), _ptr(out), M, N, K,
                                                ctypes.c_uint64(limit_ns), _stream(stream)),
           "vqlin_debug_gemm_withheld_loads")
+    return out
+
+
+def debug_w4a16_withheld_loads(X, wq, scales, zeros, group_size: int, limit_ns: int, out=None, stream=None):
+    """Failure-detection hook: the W4A16 tensor-core kernel with every tile load
+    withheld, so its bounded waits run out after limit_ns.  The error is then
+    read with get_last_device_error()."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(wq, "wq", torch.uint8, 2)
+    M, K = X.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    check(_lib.vqlin_debug_w4a16_withheld_loads(_ptr(X), _ptr(wq), _ptr(scales), _ptr(zeros), group_size,
+                                                _ptr(out), M, N, K, limit_ns, _stream(stream)),
+          "vqlin_debug_w4a16_withheld_loads")
     return out
 
 

@@ -79,9 +79,12 @@ vqlin_status launch_int_gemm_withheld(int bits, const void* xq, const void* wq, 
 cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
                               const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
                               int M, int N, int K, int* status, cudaStream_t st);
+// withhold = 1: the tile producer issues nothing, so every bounded wait runs
+// out after limit_ns (0: the default limit) -- the failure-detection test hook
 vqlin_status launch_w4a16_tc(const uint16_t* X, const uint8_t* wq, const uint16_t* s,
                              const uint16_t* z, int group, const uint16_t* bias, uint16_t* Y,
-                             int M, int N, int K, int* status, cudaStream_t st);
+                             int M, int N, int K, int* status, cudaStream_t st, int withhold = 0,
+                             uint64_t limit_ns = 0);
 constexpr int kW4a16GemvMaxM = 4;
 
 // Few-token W4A4 (lowlat_tcgen05.cu): every operand of a CTA's K range stays

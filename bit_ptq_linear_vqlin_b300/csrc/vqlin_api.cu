@@ -287,6 +287,24 @@ vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const voi
                                          static_cast<cudaStream_t>(stream));
 }
 
+vqlin_status vqlin_debug_w4a16_withheld_loads(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,
+                                              const uint16_t* zeros, int group_size, uint16_t* Y, int M, int N,
+                                              int K, uint64_t limit_ns, void* stream) {
+  REQUIRE(M > vqlin::kW4a16GemvMaxM && N > 0 && K > 0, VQLIN_ERR_INVALID_ARG,
+          "bad sizes M=%d N=%d K=%d (the tensor-core kernel takes M > %d)", M, N, K, vqlin::kW4a16GemvMaxM);
+  REQUIRE(group_size == 64 || group_size == 128 || group_size == 256, VQLIN_ERR_INVALID_ARG,
+          "group_size must be 64, 128 or 256 (got %d)", group_size);
+  REQUIRE(K % 128 == 0 && K % group_size == 0, VQLIN_ERR_UNSUPPORTED_SHAPE,
+          "K=%d must be a multiple of 128 and of the group %d", K, group_size);
+  REQUIRE(limit_ns > 0 && limit_ns <= 2000000000ull, VQLIN_ERR_INVALID_ARG, "limit_ns must be in (0, 2e9]");
+  REQUIRE_PTR(X); REQUIRE_PTR(wq); REQUIRE_PTR(scales); REQUIRE_PTR(zeros); REQUIRE_PTR(Y);
+  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(scales); REQUIRE_ALIGNED(zeros); REQUIRE_ALIGNED(Y);
+  int* status = vqlin::device_status_word();
+  REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
+  return vqlin::launch_w4a16_tc(X, wq, scales, zeros, group_size, nullptr, Y, M, N, K, status,
+                                static_cast<cudaStream_t>(stream), 1, limit_ns);
+}
+
 vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,
                                 const uint16_t* zeros, int group_size, const uint16_t* bias, uint16_t* Y,
                                 int M, int N, int K, void* stream) {

@@ -77,6 +77,7 @@ struct W4a16Args {
   int issuers;             // MMA-issuing warps (1..4), one accumulator each
   int rows_per;            // split K: output channels each cluster rank owns
   int ng_max;              // quantization groups of the CTA with the most (<= kMaxGroupsCta)
+  int withhold_loads;      // test hook: the producer issues nothing (every wait runs out)
   uint64_t wait_limit_ns;
 };
 
@@ -187,7 +188,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !a.withhold_loads) {
       int issued = 0;
       // weight tiles of the first stages before waiting for the previous
       // kernel: they are expanded into tensor memory while it still runs
@@ -462,7 +463,8 @@ size_t smem_bytes(int stages, int ng_max) {
 
 template <int BT, int GROUP>
 vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z,
-                      const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+                      const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st,
+                      int withhold, uint64_t limit_ns) {
   // function attributes are per device: set them once for every device used
   static std::mutex mu;
   static bool set[64] = {};
@@ -570,7 +572,7 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   a.scales = s; a.zeros = z; a.bias = bias; a.Y = Y; a.status = status;
   a.M = M; a.N = N; a.K = K; a.G = G; a.stages = NS; a.tmem_cols = cols; a.a_col = a_col;
   a.acc_step = acc_step; a.issuers = NI;
-  a.rows_per = rows_per; a.ng_max = ng_max; a.wait_limit_ns = kWaitLimitNs;
+  a.rows_per = rows_per; a.ng_max = ng_max; a.wait_limit_ns = limit_ns; a.withhold_loads = withhold;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_m, S);
@@ -595,11 +597,12 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
 
 template <int BT>
 vqlin_status launch_bt(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z, int group,
-                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st,
+                       int withhold, uint64_t limit_ns) {
   switch (group) {
-    case 64: return launch_t<BT, 64>(X, wq, s, z, bias, Y, M, N, K, status, st);
-    case 128: return launch_t<BT, 128>(X, wq, s, z, bias, Y, M, N, K, status, st);
-    default: return launch_t<BT, 256>(X, wq, s, z, bias, Y, M, N, K, status, st);
+    case 64: return launch_t<BT, 64>(X, wq, s, z, bias, Y, M, N, K, status, st, withhold, limit_ns);
+    case 128: return launch_t<BT, 128>(X, wq, s, z, bias, Y, M, N, K, status, st, withhold, limit_ns);
+    default: return launch_t<BT, 256>(X, wq, s, z, bias, Y, M, N, K, status, st, withhold, limit_ns);
   }
 }
 
@@ -608,15 +611,17 @@ vqlin_status launch_bt(const uint16_t* X, const uint8_t* wq, const uint16_t* s, 
 namespace vqlin {
 
 vqlin_status launch_w4a16_tc(const uint16_t* X, const uint8_t* wq, const uint16_t* s, const uint16_t* z, int group,
-                             const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st) {
+                             const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status, cudaStream_t st,
+                             int withhold, uint64_t limit_ns) {
   if (M == 0 || N == 0) return VQLIN_OK;
+  if (limit_ns == 0) limit_ns = kWaitLimitNs;
   // token tile: the smallest of 16, 32, 64 that covers M in as few tiles as
   // possible (the drain warps keep BT float sums per thread in registers)
   const int tiles = (M + 63) / 64;
   const int per = (M + tiles - 1) / tiles;
-  if (per <= 16) return launch_bt<16>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
-  if (per <= 32) return launch_bt<32>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
-  return launch_bt<64>(X, wq, s, z, group, bias, Y, M, N, K, status, st);
+  if (per <= 16) return launch_bt<16>(X, wq, s, z, group, bias, Y, M, N, K, status, st, withhold, limit_ns);
+  if (per <= 32) return launch_bt<32>(X, wq, s, z, group, bias, Y, M, N, K, status, st, withhold, limit_ns);
+  return launch_bt<64>(X, wq, s, z, group, bias, Y, M, N, K, status, st, withhold, limit_ns);
 }
 
 }  // namespace vqlin

@@ -265,6 +265,21 @@ vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const voi
                                              int M, int N, int K, uint64_t limit_ns, void* stream);
 
 /*
+ * Test entry point of failure detection for the W4A16 tensor-core kernel
+ * (M > 4, the sizes and layouts of vqlin_linear_w4a16, no bias): its tile
+ * producer withholds every load, so the weight expanders', MMA issuers' and
+ * group drains' bounded waits run out after limit_ns nanoseconds
+ * (0 < limit_ns <= 2e9).  Nothing is left in flight; the kernel records
+ * VQLIN_ERR_TIMEOUT in the device status word, frees its tensor memory and
+ * returns.  The call returns VQLIN_OK once launched; the error is read with
+ * vqlin_get_last_device_error().  Y is not written.  The pages define no such
+ * call: it exists to test the bounded waits.
+ */
+vqlin_status vqlin_debug_w4a16_withheld_loads(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,
+                                              const uint16_t* zeros, int group_size, uint16_t* Y, int M, int N,
+                                              int K, uint64_t limit_ns, void* stream);
+
+/*
  * Measurement entry point: the dense rate of one tensor-core MMA kind on this
  * GPU, the roofline denominator of the projections (no passage of the pages
  * defines it; they name no GPU figure).  kind 0: tcgen05.mma kind::f8f6f4 with

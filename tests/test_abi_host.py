@@ -94,3 +94,8 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_bf16_ref(A, A, None, A, 4, 12, 256, None) == UNSUPPORTED
     assert lib.vqlin_debug_gemm_s32(5, A, A, A, 4, 4, 256, None) == INVALID
     assert lib.vqlin_debug_gemm_s32(4, A, A, None, 4, 4, 256, None) == INVALID
+    f = lib.vqlin_debug_w4a16_withheld_loads
+    assert f(A, A, A, A, 128, A, 4, 16, 256, 1000000, None) == INVALID        # M <= 4: the GEMV, no hook
+    assert f(A, A, A, A, 128, A, 16, 16, 256, 0, None) == INVALID            # limit 0
+    assert f(A, A, A, None, 128, A, 16, 16, 256, 1000000, None) == INVALID   # null zero points
+    assert f(A, A, A, A, 128, A, 16, 16, 192, 1000000, None) == UNSUPPORTED  # K % 128

@@ -69,16 +69,31 @@ def test_traffic_lookup_follows_the_source_hash(tmp_path, monkeypatch):
 
 
 def test_work_formulas_match_the_scope_table():
-    # one launch: ops 2MNK; bytes as in the scope table's per-call formulas, with
-    # activation codes stored one byte (int4) or two bytes (int8) per code, the
-    # tensor-core operand encoding this library uses
+    # one launch: ops 2MNK; bytes as in the scope table's per-call formulas:
+    # int4 codes count half a byte each and int8 codes one byte, whatever the
+    # storage format (the storage bytes are reported beside them)
     stack = bench.ControlStepStack.__new__(bench.ControlStepStack)
     stack.group = 128
     M, N, K = 50, 1024, 4096
-    assert stack.work_of(("linear_w4a4", M, N, K)) == (2 * M * N * K, M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N)
-    assert stack.work_of(("linear_w8a8", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N)
+    assert stack.work_of(("linear_w4a4", M, N, K)) == (2 * M * N * K, M * K // 2 + N * K // 2 + 4 * M + 4 * N + 2 * M * N)
+    assert stack.work_of(("linear_w8a8", M, N, K)) == (2 * M * N * K, M * K + N * K + 4 * M + 4 * N + 2 * M * N)
     assert stack.work_of(("linear_w4a16", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K // 2 + 4 * N * K // 128
                                                         + 2 * M * N)
-    assert stack.work_of(("linear_w4a8", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N)
-    assert stack.work_of(("act_quant_static", 4, M, K)) == (0, 2 * M * K + M * K + 4 * M)
-    assert stack.work_of(("act_quant", 8, M, K)) == (0, 2 * M * K + 2 * M * K + 4 * M)
+    assert stack.work_of(("linear_w4a8", M, N, K)) == (2 * M * N * K, M * K + N * K // 2 + 4 * M + 4 * N + 2 * M * N)
+    assert stack.work_of(("linear_w4a4_static", M, N, K)) == (2 * M * N * K, 2 * M * K + N * K // 2 + 4 + 4 * N
+                                                              + 2 * M * N)
+    assert stack.work_of(("act_quant_static", 4, M, K)) == (0, 2 * M * K + M * K // 2 + 4 * M)
+    assert stack.work_of(("act_quant", 8, M, K)) == (0, 2 * M * K + M * K + 4 * M)
+    # the storage format: one byte per int4 code, two per int8 code
+    assert bench.storage_bytes("act_quant4", M, 0, K) == 2 * M * K + M * K + 4 * M
+    assert bench.storage_bytes("linear_w8a8", M, N, K) == 2 * M * K + N * K + 4 * M + 4 * N + 2 * M * N
+
+
+def test_roofline_takes_the_lower_of_the_two_ceilings():
+    # 1 TFLOP over 1 GB: ridge at 6.5 TB/s x 1000 flop/B = 6500 TFLOP/s > a 2000 TFLOP/s peak -> tensor
+    r = bench.roofline_of(1e12, 1e9, 1e6, 2000.0, 6500.0)   # 1 s
+    assert r["bound"] == "tensor" and abs(r["frac"] - 1.0 / 2000.0) < 1e-12
+    # 1 GFLOP over 1 GB: ridge 6.5 TFLOP/s -> HBM; the fraction is then the byte rate's
+    r = bench.roofline_of(1e9, 1e9, 1e3, 2000.0, 6500.0)    # 1 ms: 1000 GB/s
+    assert r["bound"] == "hbm" and abs(r["frac"] - 1000.0 / 6500.0) < 1e-9
+    assert bench.roofline_of(0, 1e9, 1e3, 2000.0, 6500.0)["bound"] == "hbm"
