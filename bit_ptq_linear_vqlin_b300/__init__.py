@@ -30,6 +30,7 @@ __all__ = [
     "quantize_weights_rtn", "act_hadamard_quant", "linear_w4a4", "linear_w4a4_static", "linear_w8a8",
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
     "debug_gemm_withheld_loads", "debug_w4a16_withheld_loads", "measure_mma_rate",
+    "composite_rotation_prepare", "quantize_weights_composite", "act_composite_quant",
     "get_last_device_error",
 ]
 
@@ -97,6 +98,50 @@ def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_o
     check(_lib.vqlin_act_hadamard_quant(_ptr(X), M, K, bits, hadamard_block, _ptr(static_scale),
                                         _ptr(q_out), _ptr(scale_out), _stream(stream)),
           "vqlin_act_hadamard_quant")
+    return q_out, scale_out
+
+
+def composite_rotation_prepare(W, block: int, stream=None):
+    """Offline: the zig-zag permutation and block rotations R_j = V_j H_b / sqrt(b)
+    of W [N, K] bf16.  Returns (perm int32 [K], R float64 [K/b, b, b])."""
+    _need(W, "W", torch.bfloat16, 2)
+    N, K = W.shape
+    perm = torch.empty((K,), dtype=torch.int32, device=W.device)
+    R = torch.empty((K // block, block, block), dtype=torch.float64, device=W.device)
+    check(_lib.vqlin_composite_rotation_prepare(_ptr(W), N, K, block, _ptr(perm), _ptr(R), _stream(stream)),
+          "vqlin_composite_rotation_prepare")
+    return perm, R
+
+
+def quantize_weights_composite(W, bits: int, block: int, perm, R, stream=None):
+    """Offline: W[:, perm] . blockdiag(R_j), per-output-channel symmetric RTN.
+    Returns (q, s) in the layout of quantize_weights_rtn."""
+    _need(W, "W", torch.bfloat16, 2)
+    _need(perm, "perm", torch.int32, 1)
+    _need(R, "R", torch.float64, 3)
+    N, K = W.shape
+    q = torch.empty((N, K // 2) if bits == 4 else (N, K), dtype=torch.uint8, device=W.device)
+    s = torch.empty((N,), dtype=torch.float32, device=W.device)
+    check(_lib.vqlin_quantize_weights_composite(_ptr(W), N, K, bits, block, _ptr(perm), _ptr(R), _ptr(q), _ptr(s),
+                                                _stream(stream)),
+          "vqlin_quantize_weights_composite")
+    return q, s
+
+
+def act_composite_quant(X, bits: int, block: int, perm, R, q_out=None, scale_out=None, stream=None):
+    """Online: X[:, perm] . blockdiag(R_j), per-token dynamic quantization.
+    Returns (q, s) in the encoding of act_hadamard_quant."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(perm, "perm", torch.int32, 1)
+    _need(R, "R", torch.float64, 3)
+    M, K = X.shape
+    if q_out is None:
+        q_out = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=X.device)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
+    check(_lib.vqlin_act_composite_quant(_ptr(X), M, K, bits, block, _ptr(perm), _ptr(R), _ptr(q_out),
+                                         _ptr(scale_out), _stream(stream)),
+          "vqlin_act_composite_quant")
     return q_out, scale_out
 
 

@@ -105,6 +105,16 @@ vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const 
 // Largest K each kernel supports (host-side shape checks).
 constexpr int kActQuantMaxK = 65536;
 constexpr int kWeightQuantMaxK = 49152;
+
+// Composite SVD . Hadamard block rotation (b = 64 or 128, K % b == 0):
+// P and R_j from the weights (float64, offline), weights rotated and
+// quantized per output channel, activations rotated and quantized per token.
+cudaError_t launch_composite_prepare(const uint16_t* W, int N, int K, int b, int* perm, double* R, int* status,
+                                     cudaStream_t st);
+cudaError_t launch_weight_quant_composite(const uint16_t* W, int N, int K, int bits, int b, const int* perm,
+                                          const double* R, uint8_t* q, float* scale, cudaStream_t st);
+cudaError_t launch_act_composite_quant(const uint16_t* X, int M, int K, int bits, int b, const int* perm,
+                                       const double* R, void* q, float* scale, cudaStream_t st);
 constexpr int kGemmW4MaxK = 65536;   // |acc| <= 49 K stays below 2^24
 constexpr int kGemmW8MaxK = 65536;   // |acc| <= 127^2 K stays below 2^31
 

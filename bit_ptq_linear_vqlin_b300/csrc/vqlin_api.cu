@@ -287,6 +287,51 @@ vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const voi
                                          static_cast<cudaStream_t>(stream));
 }
 
+vqlin_status vqlin_composite_rotation_prepare(const uint16_t* W, int N, int K, int block, int32_t* perm_out,
+                                              double* R_out, void* stream) {
+  REQUIRE(N > 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes N=%d K=%d", N, K);
+  REQUIRE(block == 64 || block == 128, VQLIN_ERR_INVALID_ARG, "block must be 64 or 128 (got %d)", block);
+  REQUIRE(K % block == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of the block %d", K, block);
+  REQUIRE(K <= vqlin::kWeightQuantMaxK, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K, vqlin::kWeightQuantMaxK);
+  REQUIRE_PTR(W); REQUIRE_PTR(perm_out); REQUIRE_PTR(R_out);
+  REQUIRE_ALIGNED(W); REQUIRE_ALIGNED(perm_out); REQUIRE_ALIGNED(R_out);
+  int* status = vqlin::device_status_word();
+  REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
+  return vqlin::check_launch(vqlin::launch_composite_prepare(W, N, K, block, perm_out, R_out, status,
+                                                             static_cast<cudaStream_t>(stream)),
+                             "composite_rotation_prepare");
+}
+
+vqlin_status vqlin_quantize_weights_composite(const uint16_t* W, int N, int K, int bits, int block,
+                                              const int32_t* perm, const double* R, void* q_out, float* scale_out,
+                                              void* stream) {
+  REQUIRE(N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes N=%d K=%d", N, K);
+  REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
+  REQUIRE(block == 64 || block == 128, VQLIN_ERR_INVALID_ARG, "block must be 64 or 128 (got %d)", block);
+  REQUIRE(K % block == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of the block %d", K, block);
+  if (N == 0) return VQLIN_OK;
+  REQUIRE_PTR(W); REQUIRE_PTR(perm); REQUIRE_PTR(R); REQUIRE_PTR(q_out); REQUIRE_PTR(scale_out);
+  REQUIRE_ALIGNED(W); REQUIRE_ALIGNED(perm); REQUIRE_ALIGNED(R); REQUIRE_ALIGNED(q_out); REQUIRE_ALIGNED(scale_out);
+  return vqlin::check_launch(vqlin::launch_weight_quant_composite(W, N, K, bits, block, perm, R,
+                                                                  static_cast<uint8_t*>(q_out), scale_out,
+                                                                  static_cast<cudaStream_t>(stream)),
+                             "quantize_weights_composite");
+}
+
+vqlin_status vqlin_act_composite_quant(const uint16_t* X, int M, int K, int bits, int block, const int32_t* perm,
+                                       const double* R, void* q_out, float* scale_out, void* stream) {
+  REQUIRE(M >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d K=%d", M, K);
+  REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
+  REQUIRE(block == 64 || block == 128, VQLIN_ERR_INVALID_ARG, "block must be 64 or 128 (got %d)", block);
+  REQUIRE(K % block == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of the block %d", K, block);
+  if (M == 0) return VQLIN_OK;
+  REQUIRE_PTR(X); REQUIRE_PTR(perm); REQUIRE_PTR(R); REQUIRE_PTR(q_out); REQUIRE_PTR(scale_out);
+  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(perm); REQUIRE_ALIGNED(R); REQUIRE_ALIGNED(q_out); REQUIRE_ALIGNED(scale_out);
+  return vqlin::check_launch(vqlin::launch_act_composite_quant(X, M, K, bits, block, perm, R, q_out, scale_out,
+                                                               static_cast<cudaStream_t>(stream)),
+                             "act_composite_quant");
+}
+
 vqlin_status vqlin_debug_w4a16_withheld_loads(const uint16_t* X, const uint8_t* wq, const uint16_t* scales,
                                               const uint16_t* zeros, int group_size, uint16_t* Y, int M, int N,
                                               int K, uint64_t limit_ns, void* stream) {

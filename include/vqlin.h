@@ -265,6 +265,44 @@ vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const voi
                                              int M, int N, int K, uint64_t limit_ns, void* stream);
 
 /*
+ * Composite SVD . Hadamard block rotation with a zig-zag channel permutation
+ * (Omega-QVLA technical summary, "Rotazione Composita SVD.Hadamard": "Rotazione
+ * SVD", "Rotazione Hadamard", "Implementazione a Blocchi").  Three calls:
+ *
+ * vqlin_composite_rotation_prepare (offline, from the bf16 weights W [N, K]):
+ *   perm_out int32 [K]: perm_out[p] = the input channel at position p of the
+ *     permuted order -- channels sorted by descending column norm (ties by
+ *     index), dealt to the K/b blocks in boustrophedon rounds (round r gives
+ *     sorted position r*nb + i to block i for even r, to nb - 1 - i for odd
+ *     r; nb = K/b), round order kept inside a block;
+ *   R_out float64 [K/b, b, b]: R_j = V_j . H_b / sqrt(b), V_j the right
+ *     singular vectors of W's columns of block j (eigenvectors of the Gram
+ *     matrix by cyclic Jacobi in float64), descending singular value, each
+ *     column signed so its largest-magnitude entry is positive.  A column set
+ *     of rank < b (N < b) has no unique null-space basis.  A Jacobi that does
+ *     not converge in 40 sweeps records VQLIN_ERR_TIMEOUT in the status word.
+ *   R_out is also the call's scratch (column norms, Gram matrices).
+ * vqlin_quantize_weights_composite (offline): W~ = W[:, perm] . blockdiag(R_j)
+ *   in float64, rounded once to float32, then per-output-channel symmetric RTN
+ *   as in vqlin_quantize_weights_rtn: q_out packed as that call's symmetric
+ *   layout ([N, K/2] int4 nibbles or [N, K] int8 bytes), scale_out float [N].
+ * vqlin_act_composite_quant (online): x~ = x[:, perm] . blockdiag(R_j) in
+ *   float32, then per-token dynamic quantization as vqlin_act_hadamard_quant:
+ *   q_out [M, K] in the activation-code encoding, scale_out float [M].
+ * The codes feed vqlin_linear_w4a4 / _w8a8 / _w4a8 unchanged: x~ . W~^T =
+ * x . W^T.  b = block in {64, 128}, K % b == 0, K <= 49152.  Every buffer is a
+ * device pointer owned by the caller, 16-byte aligned; scale_out doubles as
+ * the per-row absmax accumulator while the call runs.
+ */
+vqlin_status vqlin_composite_rotation_prepare(const uint16_t* W, int N, int K, int block, int32_t* perm_out,
+                                              double* R_out, void* stream);
+vqlin_status vqlin_quantize_weights_composite(const uint16_t* W, int N, int K, int bits, int block,
+                                              const int32_t* perm, const double* R, void* q_out, float* scale_out,
+                                              void* stream);
+vqlin_status vqlin_act_composite_quant(const uint16_t* X, int M, int K, int bits, int block, const int32_t* perm,
+                                       const double* R, void* q_out, float* scale_out, void* stream);
+
+/*
  * Test entry point of failure detection for the W4A16 tensor-core kernel
  * (M > 4, the sizes and layouts of vqlin_linear_w4a16, no bias): its tile
  * producer withholds every load, so the weight expanders', MMA issuers' and

@@ -94,6 +94,19 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_bf16_ref(A, A, None, A, 4, 12, 256, None) == UNSUPPORTED
     assert lib.vqlin_debug_gemm_s32(5, A, A, A, 4, 4, 256, None) == INVALID
     assert lib.vqlin_debug_gemm_s32(4, A, A, None, 4, 4, 256, None) == INVALID
+    f = lib.vqlin_composite_rotation_prepare
+    assert f(A, 16, 256, 32, A, A, None) == INVALID          # block size
+    assert f(A, 16, 192, 128, A, A, None) == UNSUPPORTED     # K % b
+    assert f(A, 0, 256, 64, A, A, None) == INVALID           # no weights to take the rotation from
+    assert f(A, 16, 256, 64, None, A, None) == INVALID       # null perm
+    f = lib.vqlin_quantize_weights_composite
+    assert f(A, 16, 256, 5, 64, A, A, A, A, None) == INVALID    # bits
+    assert f(A, 16, 256, 4, 64, A, None, A, A, None) == INVALID  # null R
+    assert f(A, 0, 256, 4, 64, A, A, A, A, None) == OK         # empty: no-op
+    f = lib.vqlin_act_composite_quant
+    assert f(A, 16, 320, 4, 128, A, A, A, A, None) == UNSUPPORTED   # K % b
+    assert f(A + 2, 16, 256, 8, 128, A, A, A, A, None) == MISALIGNED
+    assert f(A, 0, 256, 8, 128, A, A, A, A, None) == OK
     f = lib.vqlin_debug_w4a16_withheld_loads
     assert f(A, A, A, A, 128, A, 4, 16, 256, 1000000, None) == INVALID        # M <= 4: the GEMV, no hook
     assert f(A, A, A, A, 128, A, 16, 16, 256, 0, None) == INVALID            # limit 0
