@@ -65,11 +65,22 @@ def get_last_device_error(stream=None) -> None:
 
 
 def quantize_weights_rtn(W, bits: int, symmetric: bool = True, group_size: int = 0,
-                         hadamard_block: int = 0, stream=None):
-    """Offline RTN of W [N, K] bf16.  Returns (q, s) or, asymmetric, (q, s, z)."""
+                         hadamard_block: int = 0, stream=None, channel_scale=None):
+    """Offline RTN of W [N, K] bf16.  Returns (q, s) or, asymmetric, (q, s, z).
+    channel_scale (float32 [K], symmetric only): quantize W . diag(c)."""
     _need(W, "W", torch.bfloat16, 2)
     N, K = W.shape
     dev = W.device
+    if channel_scale is not None:
+        if not symmetric:
+            raise ValueError("channel scaling applies to the symmetric (rotated) weights")
+        _need(channel_scale, "channel_scale", torch.float32, 1)
+        q = torch.empty((N, K // 2) if bits == 4 else (N, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((N,), dtype=torch.float32, device=dev)
+        check(_lib.vqlin_quantize_weights_rtn_scaled(_ptr(W), N, K, bits, hadamard_block, _ptr(channel_scale),
+                                                     _ptr(q), _ptr(s), _stream(stream)),
+              "vqlin_quantize_weights_rtn_scaled")
+        return q, s
     q = torch.empty((N, K // 2) if bits == 4 else (N, K), dtype=torch.uint8, device=dev)
     if symmetric:
         s = torch.empty((N,), dtype=torch.float32, device=dev)
@@ -85,8 +96,9 @@ def quantize_weights_rtn(W, bits: int, symmetric: bool = True, group_size: int =
 
 
 def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_out=None,
-                       scale_out=None, stream=None):
-    """Rotate X [M, K] bf16 block-wise and quantize per token.  Returns (q, s)."""
+                       scale_out=None, stream=None, channel_scale=None):
+    """Rotate X [M, K] bf16 block-wise and quantize per token.  Returns (q, s).
+    channel_scale (float32 [K]): rotate and quantize X . diag(1/c)."""
     _need(X, "X", torch.bfloat16, 2)
     M, K = X.shape
     if q_out is None:
@@ -95,6 +107,13 @@ def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_o
         scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
     if static_scale is not None:
         _need(static_scale, "static_scale", torch.float32)
+    if channel_scale is not None:
+        _need(channel_scale, "channel_scale", torch.float32, 1)
+        check(_lib.vqlin_act_hadamard_quant_scaled(_ptr(X), M, K, bits, hadamard_block, _ptr(channel_scale),
+                                                   _ptr(static_scale), _ptr(q_out), _ptr(scale_out),
+                                                   _stream(stream)),
+              "vqlin_act_hadamard_quant_scaled")
+        return q_out, scale_out
     check(_lib.vqlin_act_hadamard_quant(_ptr(X), M, K, bits, hadamard_block, _ptr(static_scale),
                                         _ptr(q_out), _ptr(scale_out), _stream(stream)),
           "vqlin_act_hadamard_quant")

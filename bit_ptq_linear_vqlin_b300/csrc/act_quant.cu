@@ -13,7 +13,10 @@
 //     the 3 index bits inside a chunk and the 2 bits that pick the chunk are
 //     butterflied in registers and only log2(LPG) stages use warp shuffles;
 //   * the per-token absmax is reduced over the token's threads (shuffles, then
-//     shared memory across warps); one CTA holds one or more whole tokens.
+//     shared memory across warps); one CTA holds one or more whole tokens;
+//   * optional channel scaling (FoldQuantVLA abstract: channel scaling
+//     combined with the block Hadamard transform): x' = x / c per input
+//     channel, an IEEE division of each loaded value, before the rotation.
 #include "act_codes.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -33,8 +36,8 @@ struct BlockGeom {
 template <int BITS, int HB, int UPT>
 __global__ void __launch_bounds__(512)
 act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
-                 const float* __restrict__ static_scale, uint8_t* __restrict__ Q,
-                 float* __restrict__ S) {
+                 const float* __restrict__ static_scale, const float* __restrict__ chan,
+                 uint8_t* __restrict__ Q, float* __restrict__ S) {
   using Geo = BlockGeom<HB>;
   constexpr int LPG = Geo::LPG, G = Geo::G;
   constexpr int qmax = (1 << (BITS - 1)) - 1;
@@ -66,6 +69,14 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
       v[i][j][2] = bf16_lo(raw.y); v[i][j][3] = bf16_hi(raw.y);
       v[i][j][4] = bf16_lo(raw.z); v[i][j][5] = bf16_hi(raw.z);
       v[i][j][6] = bf16_lo(raw.w); v[i][j][7] = bf16_hi(raw.w);
+      if (chan != nullptr && ok) {
+        const float* cp = chan + (size_t)g * G + (l + LPG * j) * 8;
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(cp));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(cp + 4));
+        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][j][e] = __fdiv_rn(v[i][j][e], c[e]);
+      }
     }
     if (HB > 0) hadamard_unit<HB == 0 ? 128 : HB>(v[i], lane);
 #pragma unroll
@@ -122,7 +133,7 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
 }
 
 template <int BITS, int HB>
-cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, void* q, float* s,
+cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, const float* chan, void* q, float* s,
                       cudaStream_t st) {
   const int units = K / 32;
   const int upt = units <= 512 ? 1 : (units <= 1024 ? 2 : 4);  // at most 512 threads per token
@@ -148,9 +159,9 @@ cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, void* q,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   uint8_t* qb = static_cast<uint8_t*>(q);
-  if (upt == 1) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1>, X, M, K, tpr, rpc, ss, qb, s);
-  if (upt == 2) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2>, X, M, K, tpr, rpc, ss, qb, s);
-  return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4>, X, M, K, tpr, rpc, ss, qb, s);
+  if (upt == 1) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1>, X, M, K, tpr, rpc, ss, chan, qb, s);
+  if (upt == 2) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2>, X, M, K, tpr, rpc, ss, chan, qb, s);
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4>, X, M, K, tpr, rpc, ss, chan, qb, s);
 }
 
 }  // namespace
@@ -158,16 +169,16 @@ cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, void* q,
 namespace vqlin {
 
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
-                             const float* static_scale, void* q, float* s, cudaStream_t st) {
+                             const float* static_scale, void* q, float* s, cudaStream_t st, const float* chan) {
   if (M == 0) return cudaSuccess;
   if (bits == 4) {
-    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, q, s, st);
-    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, q, s, st);
-    return launch_hb<4, 128>(X, M, K, static_scale, q, s, st);
+    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, chan, q, s, st);
+    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, chan, q, s, st);
+    return launch_hb<4, 128>(X, M, K, static_scale, chan, q, s, st);
   }
-  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, q, s, st);
-  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, q, s, st);
-  return launch_hb<8, 128>(X, M, K, static_scale, q, s, st);
+  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, chan, q, s, st);
+  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, chan, q, s, st);
+  return launch_hb<8, 128>(X, M, K, static_scale, chan, q, s, st);
 }
 
 }  // namespace vqlin

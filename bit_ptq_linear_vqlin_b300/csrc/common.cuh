@@ -43,10 +43,13 @@ bool pdl_enabled();
 int max_active_clusters(const void* kernel, int threads, size_t dyn_smem, int cluster);
 
 // Launchers (defined in the kernel files).  They assume validated arguments.
+// chan: optional per-input-channel scale c [K] (x / c before the rotation;
+// for weights W * c), null for none
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
-                             const float* static_scale, void* q, float* s, cudaStream_t st);
+                             const float* static_scale, void* q, float* s, cudaStream_t st,
+                             const float* chan = nullptr);
 cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, int hb,
-                                    void* q, float* s, cudaStream_t st);
+                                    void* q, float* s, cudaStream_t st, const float* chan = nullptr);
 cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
                                      uint8_t* q, uint16_t* s, uint16_t* z, cudaStream_t st);
 // Integer GEMM (tcgen05); acc == nullptr: bf16 epilogue into Y, else raw int32

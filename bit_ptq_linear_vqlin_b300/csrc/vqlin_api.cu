@@ -131,6 +131,26 @@ vqlin_status vqlin_get_last_device_error(void* stream) {
   return VQLIN_OK;
 }
 
+vqlin_status vqlin_quantize_weights_rtn_scaled(const uint16_t* W, int N, int K, int bits, int hadamard_block,
+                                               const float* channel_scale, void* q_out, float* scale_out,
+                                               void* stream) {
+  REQUIRE(N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes N=%d K=%d", N, K);
+  REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
+  REQUIRE(hadamard_block == 0 || hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
+          "hadamard_block must be 0, 64 or 128 (got %d)", hadamard_block);
+  REQUIRE(K % 32 == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 32", K);
+  REQUIRE(hadamard_block == 0 || K % hadamard_block == 0, VQLIN_ERR_UNSUPPORTED_SHAPE,
+          "K=%d is not a multiple of the Hadamard block %d", K, hadamard_block);
+  REQUIRE(K <= vqlin::kWeightQuantMaxK, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K,
+          vqlin::kWeightQuantMaxK);
+  if (N == 0) return VQLIN_OK;
+  REQUIRE_PTR(W); REQUIRE_PTR(channel_scale); REQUIRE_PTR(q_out); REQUIRE_PTR(scale_out);
+  REQUIRE_ALIGNED(W); REQUIRE_ALIGNED(channel_scale); REQUIRE_ALIGNED(q_out); REQUIRE_ALIGNED(scale_out);
+  return vqlin::check_launch(vqlin::launch_weight_quant_sym(W, N, K, bits, hadamard_block, q_out, scale_out,
+                                                           static_cast<cudaStream_t>(stream), channel_scale),
+                             "weight_quant_sym");
+}
+
 vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bits, int symmetric,
                                         int group_size, int hadamard_block, void* q_out,
                                         void* scale_out, void* zero_out, void* stream) {
@@ -170,6 +190,13 @@ vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bit
 vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits, int hadamard_block,
                                       const float* static_scale, void* q_out, float* scale_out,
                                       void* stream) {
+  return vqlin_act_hadamard_quant_scaled(X, M, K, bits, hadamard_block, nullptr, static_scale, q_out, scale_out,
+                                         stream);
+}
+
+vqlin_status vqlin_act_hadamard_quant_scaled(const uint16_t* X, int M, int K, int bits, int hadamard_block,
+                                             const float* channel_scale, const float* static_scale, void* q_out,
+                                             float* scale_out, void* stream) {
   REQUIRE(M >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d K=%d", M, K);
   REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
   REQUIRE(hadamard_block == 0 || hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
@@ -183,8 +210,9 @@ vqlin_status vqlin_act_hadamard_quant(const uint16_t* X, int M, int K, int bits,
   REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(q_out);
   REQUIRE(vqlin::aligned16(scale_out) || (reinterpret_cast<uintptr_t>(scale_out) & 3) == 0,
           VQLIN_ERR_MISALIGNED, "scale_out is not 4-byte aligned");
+  if (channel_scale != nullptr) REQUIRE_ALIGNED(channel_scale);
   return vqlin::check_launch(vqlin::launch_act_quant(X, M, K, bits, hadamard_block, static_scale, q_out,
-                                                     scale_out, static_cast<cudaStream_t>(stream)),
+                                                     scale_out, static_cast<cudaStream_t>(stream), channel_scale),
                              "act_hadamard_quant");
 }
 

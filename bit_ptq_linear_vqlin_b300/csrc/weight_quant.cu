@@ -22,8 +22,8 @@ constexpr int kSymThreads = 256;
 
 template <int BITS>
 __global__ void __launch_bounds__(kSymThreads)
-weight_quant_sym_kernel(const uint16_t* __restrict__ W, int K, int hb, uint8_t* __restrict__ Q,
-                        float* __restrict__ S) {
+weight_quant_sym_kernel(const uint16_t* __restrict__ W, int K, int hb, const float* __restrict__ chan,
+                        uint8_t* __restrict__ Q, float* __restrict__ S) {
   constexpr int qmax = (1 << (BITS - 1)) - 1;
   extern __shared__ float rowbuf[];      // K float32 rotated values
   __shared__ double tile[kSymThreads];   // one FWHT work tile
@@ -33,13 +33,17 @@ weight_quant_sym_kernel(const uint16_t* __restrict__ W, int K, int hb, uint8_t* 
   const int t = threadIdx.x;
 
   if (hb == 0) {
-    for (int k = t; k < K; k += kSymThreads) rowbuf[k] = __uint_as_float((uint32_t)wrow[k] << 16);
+    for (int k = t; k < K; k += kSymThreads) {
+      const float w = __uint_as_float((uint32_t)wrow[k] << 16);
+      rowbuf[k] = chan != nullptr ? __double2float_rn((double)w * (double)chan[k]) : w;
+    }
   } else {
     // kSymThreads is a multiple of hb, so a tile holds whole Hadamard blocks
     const double denom = sqrt((double)hb);
     for (int k0 = 0; k0 < K; k0 += kSymThreads) {
       const int k = k0 + t;
       tile[t] = k < K ? (double)__uint_as_float((uint32_t)wrow[k] << 16) : 0.0;
+      if (chan != nullptr && k < K) tile[t] *= (double)chan[k];  // channel scaling W' = W diag(c)
       for (int h = 1; h < hb; h <<= 1) {
         __syncthreads();
         if ((t & h) == 0) {
@@ -160,7 +164,7 @@ weight_quant_asym_kernel(const uint16_t* __restrict__ W, int N, int K, uint8_t* 
 namespace vqlin {
 
 cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, int hb,
-                                    void* q, float* s, cudaStream_t st) {
+                                    void* q, float* s, cudaStream_t st, const float* chan) {
   if (N == 0) return cudaSuccess;
   const size_t smem = (size_t)K * sizeof(float);
   cudaError_t e;
@@ -168,12 +172,12 @@ cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, i
     e = cudaFuncSetAttribute(weight_quant_sym_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    weight_quant_sym_kernel<4><<<N, kSymThreads, smem, st>>>(W, K, hb, (uint8_t*)q, s);
+    weight_quant_sym_kernel<4><<<N, kSymThreads, smem, st>>>(W, K, hb, chan, (uint8_t*)q, s);
   } else {
     e = cudaFuncSetAttribute(weight_quant_sym_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    weight_quant_sym_kernel<8><<<N, kSymThreads, smem, st>>>(W, K, hb, (uint8_t*)q, s);
+    weight_quant_sym_kernel<8><<<N, kSymThreads, smem, st>>>(W, K, hb, chan, (uint8_t*)q, s);
   }
   return cudaGetLastError();
 }

@@ -108,6 +108,19 @@ vqlin_status vqlin_quantize_weights_rtn(const uint16_t* W, int N, int K, int bit
                                         void* stream);
 
 /*
+ * Channel scaling, the weight side (FoldQuantVLA abstract: channel scaling
+ * folded consistently through the rotation, the weight rounding and native
+ * integer execution): vqlin_quantize_weights_rtn, symmetric, of
+ * W' = W . diag(c) -- each weight times channel_scale[k] in float64 before the
+ * block rotation.  channel_scale: float [K] on the device, positive, finite
+ * (c[k] = 1 everywhere gives vqlin_quantize_weights_rtn).  Pair it with
+ * vqlin_act_hadamard_quant_scaled and the same c, so that x' . W'^T = x . W^T.
+ */
+vqlin_status vqlin_quantize_weights_rtn_scaled(const uint16_t* W, int N, int K, int bits, int hadamard_block,
+                                               const float* channel_scale, void* q_out, float* scale_out,
+                                               void* stream);
+
+/*
  * Online activation kernel: block-Hadamard rotation + per-token quantization.
  * (FoldQuantVLA abstract: block Hadamard transforms with dynamic per-token
  * quantization; Omega-QVLA "Scalatura delle Attivazioni DiT per Passo":
@@ -263,6 +276,17 @@ vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int3
  */
 vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const void* wq, int32_t* acc,
                                              int M, int N, int K, uint64_t limit_ns, void* stream);
+
+/*
+ * Channel scaling, the activation side (FoldQuantVLA abstract):
+ * vqlin_act_hadamard_quant of x' = x . diag(1/c) -- each loaded value divided
+ * by channel_scale[k] (IEEE float32 division) before the block rotation.
+ * channel_scale: float [K] on the device, positive, finite, or NULL for none
+ * (then exactly vqlin_act_hadamard_quant).  Other arguments as there.
+ */
+vqlin_status vqlin_act_hadamard_quant_scaled(const uint16_t* X, int M, int K, int bits, int hadamard_block,
+                                             const float* channel_scale, const float* static_scale, void* q_out,
+                                             float* scale_out, void* stream);
 
 /*
  * Composite SVD . Hadamard block rotation with a zig-zag channel permutation

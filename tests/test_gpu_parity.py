@@ -507,9 +507,16 @@ def test_output_scale_folds_ride_in_the_weight_scales(bits):
     Wb = weights(N, K, seed=72)
     f = sf.head_factors(np.array([1.0, 1.3, 0.75, 1.1]), N // 4)
     wq, sw = vq.quantize_weights_rtn(to_dev_bf16(Wb), bits, True, 0, hb)
-    sw_folded = sw * torch.from_numpy(f.astype(np.float32)).to(DEV)
+    # the fold itself is offline arithmetic: the oracle's s_w' = float32(s_w * f)
+    sw_folded = torch.from_numpy(sf.fold_output_scales(sw.cpu().numpy(), f)).to(DEV)
     xq, sx = vq.act_hadamard_quant(to_dev_bf16(Xb), bits, hb)
     fn = vq.linear_w4a4 if bits == 4 else vq.linear_w8a8
     y = fn(xq, sx, wq, sw_folded)
     ref = sf.linear_quantized_scaled(Xb, Wb, bits, hb, out_factor=f)
     assert rel_fro(bf16_bits(y), ref["y"]) <= 1e-3
+    # with the oracle's own codes and folded scales, the epilogue is within
+    # one bf16 ulp of the oracle's float64 epilogue
+    y2 = fn(encode_act(ref["xq"], bits), torch.from_numpy(ref["sx"]).to(DEV), pack_codes(ref["wq"], bits),
+            torch.from_numpy(ref["sw"]).to(DEV))
+    ulp = np.abs(bf16_bits(y2).astype(np.int64) - ref["y"].astype(np.int64))
+    assert ulp.max() <= 1 and (ulp > 0).mean() < 0.01
