@@ -31,6 +31,7 @@ __all__ = [
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
     "debug_gemm_withheld_loads", "debug_w4a16_withheld_loads", "measure_mma_rate",
     "composite_rotation_prepare", "quantize_weights_composite", "act_composite_quant",
+    "init", "shutdown",
     "get_last_device_error",
 ]
 
@@ -57,6 +58,17 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def init() -> None:
+    """Create the library's per-device state now (status word, cuBLASLt handle
+    and workspace) instead of on first use."""
+    check(_lib.vqlin_init(), "vqlin_init")
+
+
+def shutdown() -> None:
+    """Release the library's per-device state (after each device's queued work)."""
+    check(_lib.vqlin_shutdown(), "vqlin_shutdown")
 
 
 def get_last_device_error(stream=None) -> None:

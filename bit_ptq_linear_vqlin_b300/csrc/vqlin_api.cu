@@ -3,7 +3,8 @@
 // Every entry point checks its arguments on the host and launches nothing
 // when they are invalid.  No entry point allocates per call; the only device
 // memory the library owns is the cuBLASLt workspace of the bf16 baseline,
-// created once per device on first use.
+// created once per device by vqlin_init() or on first use, and released by
+// vqlin_shutdown().
 #include <cstdarg>
 #include <cstdio>
 #include <map>
@@ -85,6 +86,34 @@ int* device_status_word() {
 }
 
 }  // namespace vqlin
+
+extern "C" vqlin_status vqlin_init(void) {
+  vqlin::DeviceState* s = nullptr;
+  return vqlin::device_state(&s, true);
+}
+
+extern "C" vqlin_status vqlin_shutdown(void) {
+  int cur = -1;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  vqlin_status out = VQLIN_OK;
+  std::lock_guard<std::mutex> lock(vqlin::g_mu);
+  for (int d = 0; d < 64; ++d) {
+    vqlin::DeviceState& s = vqlin::g_dev[d];
+    if (!s.ready) continue;
+    // the handle and workspace may still be in use by queued work on that device
+    if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      out = vqlin::fail(VQLIN_ERR_CUDA, "vqlin_shutdown: device %d did not synchronise", d);
+    if (s.lt != nullptr) cublasLtDestroy(s.lt);
+    if (s.workspace != nullptr) cudaFree(s.workspace);
+    s.lt = nullptr;
+    s.workspace = nullptr;
+    s.workspace_bytes = 0;
+    s.algos.clear();
+    s.ready = false;
+  }
+  if (have_cur) cudaSetDevice(cur);
+  return out;
+}
 
 using vqlin::fail;
 

@@ -82,6 +82,24 @@ const char* vqlin_last_error_message(void);
 vqlin_status vqlin_get_last_device_error(void* stream);
 
 /*
+ * Library state of the current device, made ahead of the first call: the
+ * device status word's address and the cuBLASLt handle and 64 MiB workspace of
+ * the bf16 baseline (vqlin_linear_bf16_ref).  Optional -- every call creates
+ * what it needs on first use -- but calling it before capturing a CUDA graph
+ * or timing keeps that one-time work out of them.  Returns VQLIN_ERR_CUDA if
+ * there is no usable device.  The pages define no such call.
+ */
+vqlin_status vqlin_init(void);
+
+/*
+ * Releases what vqlin_init (or first use) created on every device: waits for
+ * each such device's queued work, then destroys its cuBLASLt handle and frees
+ * its workspace.  Device memory the caller owns is untouched.  A later call
+ * creates the state again.  Must not run concurrently with other calls.
+ */
+vqlin_status vqlin_shutdown(void);
+
+/*
  * Offline weight preparation: round-to-nearest quantization of W [N, K] bf16.
  * ("plain RTN", LoopQ abstract; rotation folded into the weights,
  * FoldQuantVLA abstract and Omega-QVLA "Rotazione Hadamard".)
@@ -224,8 +242,11 @@ vqlin_status vqlin_linear_w4a4_static_noalloc(const uint16_t* X, const float* st
                                               const uint16_t* bias, uint16_t* Y, int M, int N, int K,
                                               void* stream);
 
-/* W8A8 projection: as vqlin_linear_w4a4 with int8 activation codes xq
- * [M, K] uint16 and int8 weight codes wq [N, K] bytes (exact f16 operands;
+/* W8A8 projection (FoldQuantVLA abstract: the attention-output and
+ * feed-forward down projections kept at eight bits, native integer execution
+ * with dynamic per-token activations): as vqlin_linear_w4a4 with int8
+ * activation codes xq [M, K] uint16 and int8 weight codes wq [N, K] bytes
+ * (exact f16 operands;
  * float32 partial sums cover at most 1024 channels, which bounds them below
  * 2^24, and are added up in int32).  Requires K % 64 == 0 and K <= 65536. */
 vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_t* wq,
@@ -233,7 +254,9 @@ vqlin_status vqlin_linear_w8a8(const uint16_t* xq, const float* sx, const uint8_
                                int M, int N, int K, void* stream);
 
 /*
- * W4A16 projection (weight-only int4, group-wise asymmetric):
+ * W4A16 projection (weight-only int4, group-wise asymmetric; LoopQ abstract:
+ * the batch-1 action expert is memory-bound, so weight bytes dominate and
+ * plain RTN weight-only quantization targets it):
  *   Wdq[n,k] = (q[n,k] - z[n,k/g]) * s[n,k/g];
  *   Y = bf16( sum_k X[m,k] * Wdq[n,k] + bias[n] ), float32 accumulation.
  * X: bf16 [M, K]; wq: uint4 [N, K/2]; scales, zeros: bf16 [N, K/g];
@@ -245,8 +268,9 @@ vqlin_status vqlin_linear_w4a16(const uint16_t* X, const uint8_t* wq, const uint
                                 uint16_t* Y, int M, int N, int K, void* stream);
 
 /*
- * 16-bit baseline projection (cuBLAS): Y = bf16(X . W^T + bias), float32
- * accumulation.  X: bf16 [M, K]; W: bf16 [N, K]; bias: bf16 [N] or NULL.
+ * 16-bit baseline projection (cuBLAS; LoopQ abstract: the 16-bit model the
+ * quantized ones are timed against; FoldQuantVLA abstract: the floating-point
+ * baseline): Y = bf16(X . W^T + bias), float32 accumulation.  X: bf16 [M, K]; W: bf16 [N, K]; bias: bf16 [N] or NULL.
  * Requires K % 8 == 0 and N % 8 == 0.
  */
 vqlin_status vqlin_linear_bf16_ref(const uint16_t* X, const uint16_t* W, const uint16_t* bias,

@@ -70,6 +70,11 @@ def test_weight_quant_rejects_bad_arguments(lib):
     assert f(A, 8, 256, 4, 1, 0, 0, A + 2, A, None, None) == MISALIGNED
 
 
+def test_shutdown_without_state_is_a_no_op(lib):
+    # nothing was created on this host (no device): there is nothing to release
+    assert lib.vqlin_shutdown() == OK
+
+
 def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED
     assert lib.vqlin_linear_w8a8(A, A, A, A, None, A, 16, 16, 96, None) == UNSUPPORTED
