@@ -101,6 +101,8 @@ vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_sc
                                        const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
                                        int N, int K, int* status, cudaStream_t st);
 // The same kernel fed with the activation kernel's codes and per-token scales.
+// Whether the few-token W4A4 kernel's plan fits one wave of clusters.
+bool lowlat_one_wave(bool fused, int hb, int M, int N, int K);
 vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
                                       cudaStream_t st);

@@ -658,6 +658,34 @@ vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_sc
   return launch_lowlat<true, 128>(X, static_scale, nullptr, nullptr, xq_ws, wq, sw, bias, Y, M, N, K, status, st);
 }
 
+// Whether the few-token kernel's plan runs as one wave of clusters: the kernel
+// stages a CTA's whole K range of weights on chip before it waits for the
+// previous launch, which pays off only when every CTA is resident at once
+// (beyond that, its fixed per-CTA cost repeats every wave and the throughput
+// GEMM streams the weights faster).
+bool lowlat_one_wave(bool fused, int hb, int M, int N, int K) {
+  LowlatPlan p;
+  bool ok;
+  int active = 0;
+  cudaError_t ae = cudaSuccess;
+  if (fused && hb == 64) {
+    set_attrs_once<true, 64>(&ae);
+    ok = ae == cudaSuccess && make_plan<true, 64>(M, N, K, p);
+    if (ok) active = max_active_clusters((const void*)w4a4_lowlat_kernel<true, 64>, kThreads, p.dyn, p.cn * p.S);
+  } else if (fused) {
+    set_attrs_once<true, 128>(&ae);
+    ok = ae == cudaSuccess && make_plan<true, 128>(M, N, K, p);
+    if (ok) active = max_active_clusters((const void*)w4a4_lowlat_kernel<true, 128>, kThreads, p.dyn, p.cn * p.S);
+  } else {
+    set_attrs_once<false, 128>(&ae);
+    ok = ae == cudaSuccess && make_plan<false, 128>(M, N, K, p);
+    if (ok) active = max_active_clusters((const void*)w4a4_lowlat_kernel<false, 128>, kThreads, p.dyn, p.cn * p.S);
+  }
+  if (!ok) return false;
+  const long long clusters = (long long)(p.tiles_n_pad / p.cn) * p.tiles_m;
+  return clusters <= active;
+}
+
 vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
                                       cudaStream_t st) {
@@ -741,7 +769,7 @@ extern "C" vqlin_status vqlin_linear_w4a4_static_noalloc(const uint16_t* X, cons
   if (r != VQLIN_OK) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the same dispatch as vqlin_linear_w4a4_static, the code buffer being the array
-  if (K <= vqlin::kLowlatMaxK)
+  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K))
     return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, codes, wq, sw, bias, Y, M, N, K, status,
                                             st);
   const cudaError_t e = vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, codes, nullptr, st);

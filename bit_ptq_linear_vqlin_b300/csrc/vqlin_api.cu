@@ -269,7 +269,8 @@ static vqlin_status linear_int(int bits, const void* xq, const float* sx, const 
     return vqlin::launch_int_gemm_w4a8(xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
                                        static_cast<cudaStream_t>(stream));
   // few tokens: the kernel that keeps every operand of its K range on chip
-  if (bits == 4 && acc == nullptr && M <= vqlin::kLowlatMaxM && K <= vqlin::kLowlatMaxK)
+  if (bits == 4 && acc == nullptr && M <= vqlin::kLowlatMaxM && K <= vqlin::kLowlatMaxK &&
+      vqlin::lowlat_one_wave(false, 128, M, N, K))
     return vqlin::launch_w4a4_codes_lowlat(static_cast<const uint8_t*>(xq), sx, static_cast<const uint8_t*>(wq), sw,
                                            bias, Y, M, N, K, status, static_cast<cudaStream_t>(stream));
   return vqlin::launch_int_gemm(bits, xq, sx, wq, sw, bias, Y, acc, M, N, K, status,
@@ -311,10 +312,11 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K <= vqlin::kLowlatMaxK)
+  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K))
     return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, xq_out, wq, sw, bias, Y, M, N, K,
                                             status, st);
-  // longer K: the activation kernel writes the codes, the throughput GEMM uses them
+  // longer K or more than one wave: the activation kernel writes the codes,
+  // the throughput GEMM uses them
   vqlin_status r = vqlin::check_launch(
       vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st), "act_hadamard_quant");
   if (r != VQLIN_OK) return r;
