@@ -56,9 +56,12 @@ def parse_args(argv=None):
                     help="prefix tokens per projection in the CPU-oracle sample")
     ap.add_argument("--skip-shapes", action="store_true",
                     help="leave out the per-shape lines (configs 1-4) after the control step")
+    ap.add_argument("--skip-cpu", action="store_true",
+                    help="leave out the CPU-oracle leg (cpu_baseline null), e.g. for profiler runs")
     ap.add_argument("--shape", default=None,
                     help="time one kernel class alone instead of the control step: KIND,M,N,K with KIND in "
-                         "act_quant4, act_quant8, act_quant_static4, linear_w4a4, linear_w4a4_static, linear_w8a8, linear_w4a8, "
+                         "act_quant4, act_quant8, act_quant_static4, act_composite4, act_composite8, linear_w4a4, "
+                         "linear_w4a4_static, linear_w8a8, linear_w4a8, "
                          "linear_w4a16, "
                          "linear_bf16 "
                          "(N is ignored for act_quant); prints a per-shape JSON line")
@@ -713,7 +716,7 @@ def run_vqlin(args):
 
     # -- CPU oracle baseline (rank 0 only): all cores and one thread
     cpu = None
-    if rank == 0:
+    if rank == 0 and not args.skip_cpu:
         prep = oracle_prepare(args.seed, args.cpu_sample_rows)
         runs = [oracle_run(prep) for _ in range(3)]
         per_step = sum(r[0] for r in runs) / len(runs)
@@ -1065,7 +1068,18 @@ def run_shape(args):
         return (mag | (sgn << 15)).to(torch.int16)
 
     group = 128
-    if kind.startswith("act_quant"):
+    if kind.startswith("act_composite"):
+        # composite SVD.Hadamard rotation (block 128) of activations: P and R_j
+        # prepared offline from a K x K weight, then rotated and quantized
+        bits = int(kind[-1])
+        per = 2 * M * K
+        flops, nbytes = 2 * M * K * 128, 2 * M * K + M * K * (1 if bits == 4 else 2) + 4 * M
+        perm, R = vq.composite_rotation_prepare(rand_bf16(K, K), 128)
+        mk = lambda: dict(X=rand_bf16(M, K))  # noqa: E731
+        q = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=dev)
+        sx = torch.empty(M, device=dev)
+        run = lambda d: vq.act_composite_quant(d["X"], bits, 128, perm, R, q_out=q, scale_out=sx)  # noqa: E731
+    elif kind.startswith("act_quant"):
         # act_quant4 / act_quant8: dynamic per-token scales; act_quant_static4: one static scale
         bits = int(kind[-1])
         per = 2 * M * K
@@ -1118,7 +1132,7 @@ def run_shape(args):
         raise SystemExit(f"unknown kernel class {kind}")
 
     # algorithmic bytes of the scope table (int4 codes MK/2, int8 codes MK)
-    nbytes = alg_bytes(("act_quant" + kind[-1]) if kind.startswith("act_quant") else kind, M, N, K, group)
+    nbytes = alg_bytes(("act_quant" + kind[-1]) if kind.startswith("act_") else kind, M, N, K, group)
     copies = max(2, min(64, -(-2 * l2 // max(per, 1))))
     data = [mk() for _ in range(copies)]
 
