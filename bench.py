@@ -244,6 +244,8 @@ def oracle_tie_fraction(prep, vq, torch, dev):
 
 
 def blas_threads() -> int:
+    """Threads of the BLAS pool numpy uses: threadpoolctl's count where it is
+    installed, else the pool size the environment requests, else the cores."""
     try:
         import threadpoolctl
         n = sum(i.get("num_threads", 0) for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas")
@@ -251,6 +253,9 @@ def blas_threads() -> int:
             return n
     except Exception:
         pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
     return os.cpu_count() or 1
 
 
