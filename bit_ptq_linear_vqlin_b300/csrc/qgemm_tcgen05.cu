@@ -760,13 +760,23 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   constexpr int NT = (FX || BITS == 8) ? kThreadsFx : kThreads;
   const auto kern = qgemm_kernel<BITS, FX, HB, W4>;
   constexpr int RAW = (BITS == 8 && W4) ? 32 : kRawRow;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [kern] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
+  // function attributes are per device: set them once for every device used
+  static std::mutex attr_mu;
+  static bool attr_set[64] = {};
+  static cudaError_t attr_res[64] = {};
+  cudaError_t attr_err = cudaSuccess;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: no device");
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev]) {
+      attr_res[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      if (attr_res[dev] == cudaSuccess)
+        attr_res[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_set[dev] = true;
+    }
+    attr_err = attr_res[dev];
+  }
   if (attr_err != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
 
