@@ -800,11 +800,12 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   // chunked: int8 beyond 1024 channels keeps two float32 accumulators and an
   // int32 running sum in tensor memory (token tile <= 128); otherwise every
   // CTA sums at most s_min-th of K (int8: <= 1024 channels)
-  auto make_plan = [&](bool chunked, int s_min, Plan& p) -> bool {
+  auto make_plan = [&](bool chunked, int s_min, Plan& p, int bt_force) -> bool {
     const int bt_max = chunked ? 128 : 256;
     const int nt = (M + bt_max - 1) / bt_max;
-    const int bt = ((M + nt - 1) / nt + 15) / 16 * 16;
-    const int tiles_n = (N + kTileN - 1) / kTileN, tiles_m = (M + bt - 1) / bt;
+    const int bt = bt_force > 0 ? bt_force : ((M + nt - 1) / nt + 15) / 16 * 16;
+    const int tiles_n = (N + kTileN - 1) / kTileN;
+    const int tiles_m = (M + bt - 1) / bt;
     int s_want = (148 + tiles_n * tiles_m - 1) / (tiles_n * tiles_m);
     s_want = s_want < s_min ? s_min : s_want;
     s_want = s_want > kMaxSplit ? kMaxSplit : s_want;
@@ -874,20 +875,50 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
     }
     return found;
   };
+  // Many tokens on fewer tiles than SMs: also try the token tile (>= 96)
+  // that puts the most CTAs in one wave, and keep it if a k-block-paced
+  // estimate (0.25 us per k-block at 6 stages or more, longer with fewer,
+  // + 0.0004 bt; a split adds 1.2 + 0.03 bt + 0.17 S us) is 5% lower.
+  // Timed on B300: W8A8 816 x 2048 x 16384 85.9 -> 70.6 us (96 tokens, 144
+  // CTAs, 6 stages instead of 4); W4A4 816 x 2560 x 2048 9.9 -> 8.7 us (128
+  // tokens, 140 CTAs); W4A4 512 x 4096 x 4096 17.5 -> 13.3 us (160 tokens,
+  // unsplit instead of split 2); a long K keeps its split (W4A8 512 x 4096 x
+  // 11008: 37 us split against 54 us at 160 tokens unsplit).
+  auto pick = [&](bool chunked, int s_min, Plan& out) -> bool {
+    if (!make_plan(chunked, s_min, out, 0)) return false;
+    if (M < 256 || out.tiles_n * out.tiles_m >= 148) return true;
+    const int bt_max = chunked ? 128 : 256;
+    int bt_fill = out.bt, best_tiles = out.tiles_n * out.tiles_m;
+    for (int c = bt_max; c >= 96; c -= 16) {
+      const int t = out.tiles_n * ((M + c - 1) / c);
+      if (t <= 148 && t > best_tiles) {
+        best_tiles = t;
+        bt_fill = c;
+      }
+    }
+    Plan alt;
+    if (bt_fill == out.bt || !make_plan(chunked, s_min, alt, bt_fill) || !alt.one_wave) return true;
+    auto est = [&](const Plan& q) {
+      const double t_kb = 0.25 * (q.NS >= 6 ? 1.0 : 6.0 / q.NS) + 0.0004 * q.bt;
+      return ((nkb + q.S - 1) / q.S) * t_kb + (q.S > 1 ? 1.2 + 0.03 * q.bt + 0.17 * q.S : 0.0);
+    };
+    if (est(alt) < 0.95 * est(out)) out = alt;
+    return true;
+  };
   Plan plan;
   bool have = false;
   if (BITS == 8 && K > exact_ch) {
     // int8 activations: split K over a cluster so no CTA sums more than
     // exact_ch channels if that runs in one wave, else chunk inside each CTA
     Plan split;
-    if (make_plan(false, (K + exact_ch - 1) / exact_ch, split) && split.one_wave) {
+    if (pick(false, (K + exact_ch - 1) / exact_ch, split) && split.one_wave) {
       plan = split;
       have = true;
     } else {
-      have = make_plan(true, 1, plan);
+      have = pick(true, 1, plan);
     }
   } else {
-    have = make_plan(false, 1, plan);
+    have = pick(false, 1, plan);
   }
   if (!have) return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "qgemm: no tile plan for M=%d N=%d K=%d", M, N, K);
   const bool chunked = plan.chunked;
