@@ -269,6 +269,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// 4-byte store into the shared memory of a cluster peer (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // 16-byte load from the shared memory of a cluster peer (address from mapa).
 __device__ __forceinline__ float4 ld_shared_cluster_v4f(uint32_t addr) {
   float4 v;

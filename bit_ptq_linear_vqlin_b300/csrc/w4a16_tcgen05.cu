@@ -110,6 +110,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_bias[kTileN];  // split K: the tile's bias, read by the reducing threads
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int NS = a.stages;
@@ -183,6 +184,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const int row = (warp & 3) * 32 + lane, n = n0 + row;
     for (int g = half; g < ng; g += 2) ssm[g * kTileN + row] = n < a.N ? __ldg(a.scales + (size_t)n * a.G + g0 + g) : 0;
     if (S == 1 && a.bias != nullptr && n < a.N) bias_r = __uint_as_float((uint32_t)__ldg(a.bias + n) << 16);
+    if (S > 1 && half == 0)
+      s_bias[row] = (a.bias != nullptr && n < a.N) ? __uint_as_float((uint32_t)__ldg(a.bias + n) << 16) : 0.0f;
     named_barrier(2, kDrainThreads);
   }
 
@@ -389,45 +392,41 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     tc_fence_before();
     __syncthreads();
   } else {
-    // float partial tile part[token][channel] over the idle stages
+    // Split K: each drain thread stores its partial row straight into the
+    // shared memory of the cluster rank that owns the row (posted stores, no
+    // round trip), as part[src][token][local row] over the owner's idle
+    // stages; after the second cluster barrier every rank sums its rows'
+    // slices from its own shared memory in source order (deterministic).
     float* part = reinterpret_cast<float*>(base);
-    __syncthreads();  // every role is past the stages before they are overwritten
+    const int rows_per = a.rows_per;
+    tc_fence_before();
+    cluster_sync_all();  // every CTA of the cluster is past its stages before they are overwritten
     if (drain && !*abort && ncol > 0) {
       const int row = (warp & 3) * 32 + lane;
+      const int owner = row / rows_per, lrow = row - owner * rows_per;
+      const uint32_t dst = mapa_shared(smem_addr(part + ((size_t)rank * BT + 32 * half) * rows_per + lrow),
+                                       (uint32_t)owner);
 #pragma unroll
       for (int c = 0; c < kHalfCols; ++c)
-        if (c < ncol) part[(32 * half + c) * kTileN + row] = y[c];
+        if (c < ncol) st_shared_cluster_f32(dst + (uint32_t)(c * rows_per * 4), y[c]);
     }
-    tc_fence_before();
     cluster_sync_all();
     if (!*abort) {
-      const int rows_per = a.rows_per;
       const int r0 = (int)rank * rows_per;
       const int nq = (min(kTileN, r0 + rows_per) - r0) / 4;
-      const uint32_t part_s = smem_addr(part);
       const bool vec = (a.N & 3) == 0;
       for (int idx = tid; idx < nq * BT; idx += kThreads) {
-        const int rr = r0 + 4 * (idx % nq), col = idx / nq;
-        const int m = m0 + col, n = n0 + rr;
+        const int lr = 4 * (idx % nq), col = idx / nq;
+        const int m = m0 + col, n = n0 + r0 + lr;
         if (m >= a.M || n >= a.N) continue;
-        const uint32_t off = (uint32_t)(col * kTileN + rr) * 4u;
-        float4 pv[kMaxSplit];
-#pragma unroll
-        for (int cc = 0; cc < kMaxSplit; ++cc)
-          if (cc < S) pv[cc] = ld_shared_cluster_v4f(mapa_shared(part_s + off, (uint32_t)cc));
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int cc = 0; cc < kMaxSplit; ++cc)
-          if (cc < S) {
-            acc[0] += pv[cc].x; acc[1] += pv[cc].y; acc[2] += pv[cc].z; acc[3] += pv[cc].w;
-          }
+        for (int cc = 0; cc < S; ++cc) {
+          const float4 pv = *reinterpret_cast<const float4*>(part + ((size_t)cc * BT + col) * rows_per + lr);
+          acc[0] += pv.x; acc[1] += pv.y; acc[2] += pv.z; acc[3] += pv.w;
+        }
         uint16_t yo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float b = (a.bias != nullptr && n + e < a.N) ? __uint_as_float((uint32_t)__ldg(a.bias + n + e) << 16)
-                                                              : 0.0f;
-          yo[e] = f32_to_bf16_rn(__fadd_rn(acc[e], b));
-        }
+        for (int e = 0; e < 4; ++e) yo[e] = f32_to_bf16_rn(__fadd_rn(acc[e], s_bias[r0 + lr + e]));
         uint16_t* dst = a.Y + (size_t)m * a.N + n;
         if (vec) {
           *reinterpret_cast<uint2*>(dst) =
@@ -437,7 +436,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
       }
     }
-    cluster_sync_all();
   }
   if (warp == 1) {
     if (!mbar_wait_bounded(done, 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
@@ -514,7 +512,10 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     const int per_cta = groups * (GROUP / kKB);
     // stages: up to 8, no more than the k-blocks a CTA runs, and enough that
     // the float partial tile of the split-K epilogue ([BT][128]) fits over them
-    const int ns_min = (int)(((size_t)BT * kTileN * 4 + stage_bytes<BT>() - 1) / stage_bytes<BT>());
+    // (split K: s_try slices of [BT][rows_per] floats, rows_per rounded up to 4)
+    const int rp_try = s_try > 1 ? ((kTileN + s_try - 1) / s_try + 3) & ~3 : kTileN;
+    const size_t part_bytes = (size_t)(s_try > 1 ? s_try * rp_try : kTileN) * BT * 4;
+    const int ns_min = (int)((part_bytes + stage_bytes<BT>() - 1) / stage_bytes<BT>());
     int ns = per_cta > 8 ? 8 : per_cta;
     if (ns < ns_min) ns = ns_min;
     if (ns < 2) ns = 2;
