@@ -103,9 +103,13 @@ vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_sc
 // The same kernel fed with the activation kernel's codes and per-token scales.
 // Whether the few-token W4A4 kernel's plan fits one wave of clusters.
 bool lowlat_one_wave(bool fused, int hb, int M, int N, int K);
+// sx_step 1: per-token scales sx[m]; 0: one scale sx[0] for every token
 vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
-                                      cudaStream_t st);
+                                      cudaStream_t st, int sx_step = 1);
+// Whether the static-scale projection at this K runs as the activation kernel
+// plus the codes variant instead of the one-launch kernel.
+bool static_two_launch(int K);
 
 // Largest K each kernel supports (host-side shape checks).
 constexpr int kActQuantMaxK = 65536;

@@ -67,7 +67,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 struct LowlatArgs {
   const uint16_t* X;            // FUSED: bf16 activations [M, K]
   const float* static_scale;    // FUSED: one device float
-  const float* sx;              // codes variant: per-token scales [M]
+  const float* sx;              // codes variant: per-token scales [M] (sx_step 1) or one scale (0)
+  int sx_step;
   const float* sw;
   const uint16_t* bias;
   uint16_t* Y;
@@ -295,7 +296,7 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
           s_sw[i] = wv[q];
           s_bias[i] = bv[q];
         }
-        if (i < 128) s_sx[i] = i < mt ? (FUSED ? xs : __ldg(a.sx + m0 + i)) * su : 0.0f;
+        if (i < 128) s_sx[i] = i < mt ? (FUSED ? xs : __ldg(a.sx + (size_t)(m0 + i) * a.sx_step)) * su : 0.0f;
       }
       mbar_arrive(scl_ready);
     }
@@ -601,7 +602,7 @@ bool make_plan(int M, int N, int K, LowlatPlan& p) {
 template <bool FUSED, int HB>
 vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const uint8_t* xq_in, const float* sx,
                            uint8_t* xq_ws, const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y,
-                           int M, int N, int K, int* status, cudaStream_t st) {
+                           int M, int N, int K, int* status, cudaStream_t st, int sx_step = 1) {
   cudaError_t ae = cudaSuccess;
   set_attrs_once<FUSED, HB>(&ae);
   if (ae != cudaSuccess)
@@ -620,7 +621,8 @@ vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const u
   if (!ok) return vqlin::fail(VQLIN_ERR_CUDA, "w4a4 low-latency: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
 
   LowlatArgs a;
-  a.X = X; a.static_scale = static_scale; a.sx = sx; a.sw = sw; a.bias = bias; a.Y = Y; a.xq = xq_ws;
+  a.X = X; a.static_scale = static_scale; a.sx = sx; a.sx_step = sx_step; a.sw = sw; a.bias = bias; a.Y = Y;
+  a.xq = xq_ws;
   a.status = status; a.M = M; a.N = N; a.K = K; a.bt = p.bt; a.nkb = K / 128; a.cn = p.cn;
   a.tmem_cols = p.cols; a.rows_per = p.rows_per; a.issuers = p.issuers; a.wait_limit_ns = kWaitLimitNs;
 
@@ -688,10 +690,17 @@ bool lowlat_one_wave(bool fused, int hb, int M, int N, int K) {
 
 vqlin_status launch_w4a4_codes_lowlat(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                                       const uint16_t* bias, uint16_t* Y, int M, int N, int K, int* status,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, int sx_step) {
   if (M == 0 || N == 0) return VQLIN_OK;
-  return launch_lowlat<false, 128>(nullptr, nullptr, xq, sx, nullptr, wq, sw, bias, Y, M, N, K, status, st);
+  return launch_lowlat<false, 128>(nullptr, nullptr, xq, sx, nullptr, wq, sw, bias, Y, M, N, K, status, st,
+                                   sx_step);
 }
+
+// Static-scale projection at long K: at 32 k-blocks or more the one-launch
+// kernel's on-chip quantization and code exchange (spread over a split of 4
+// or more) cost more than the activation kernel plus the codes variant
+// (B300, 50 x 1024 x 4096: 10.1 us against about 8 us); below, one launch wins.
+bool static_two_launch(int K) { return K / 128 >= 32; }
 
 }  // namespace vqlin
 
@@ -769,9 +778,16 @@ extern "C" vqlin_status vqlin_linear_w4a4_static_noalloc(const uint16_t* X, cons
   if (r != VQLIN_OK) return r;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the same dispatch as vqlin_linear_w4a4_static, the code buffer being the array
-  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K))
-    return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, codes, wq, sw, bias, Y, M, N, K, status,
-                                            st);
+  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K)) {
+    if (!vqlin::static_two_launch(K))
+      return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, codes, wq, sw, bias, Y, M, N, K,
+                                              status, st);
+    if (vqlin::lowlat_one_wave(false, 128, M, N, K)) {
+      const cudaError_t e = vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, codes, nullptr, st);
+      if (e != cudaSuccess) return vqlin::fail(VQLIN_ERR_CUDA, "act_hadamard_quant: %s", cudaGetErrorString(e));
+      return vqlin::launch_w4a4_codes_lowlat(codes, static_scale, wq, sw, bias, Y, M, N, K, status, st, 0);
+    }
+  }
   const cudaError_t e = vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, codes, nullptr, st);
   if (e != cudaSuccess) return vqlin::fail(VQLIN_ERR_CUDA, "act_hadamard_quant: %s", cudaGetErrorString(e));
   return vqlin::launch_int_gemm_static_scale(codes, static_scale, wq, sw, bias, Y, M, N, K, status, st);

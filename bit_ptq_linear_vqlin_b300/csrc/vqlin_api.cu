@@ -312,9 +312,18 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K))
-    return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, xq_out, wq, sw, bias, Y, M, N, K,
-                                            status, st);
+  if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K)) {
+    if (!vqlin::static_two_launch(K))
+      return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, xq_out, wq, sw, bias, Y, M, N, K,
+                                              status, st);
+    if (vqlin::lowlat_one_wave(false, 128, M, N, K)) {
+      // long K: the activation kernel, then the few-token GEMM on its codes
+      vqlin_status r = vqlin::check_launch(
+          vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st), "act_hadamard_quant");
+      if (r != VQLIN_OK) return r;
+      return vqlin::launch_w4a4_codes_lowlat(xq_out, static_scale, wq, sw, bias, Y, M, N, K, status, st, 0);
+    }
+  }
   // longer K or more than one wave: the activation kernel writes the codes,
   // the throughput GEMM uses them
   vqlin_status r = vqlin::check_launch(
