@@ -31,7 +31,7 @@ __all__ = [
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
     "debug_gemm_withheld_loads", "debug_w4a16_withheld_loads", "measure_mma_rate",
     "composite_rotation_prepare", "quantize_weights_composite", "act_composite_quant",
-    "init", "shutdown",
+    "init", "shutdown", "act_adaln_hadamard_quant",
     "get_last_device_error",
 ]
 
@@ -129,6 +129,28 @@ def act_hadamard_quant(X, bits: int, hadamard_block: int, static_scale=None, q_o
     check(_lib.vqlin_act_hadamard_quant(_ptr(X), M, K, bits, hadamard_block, _ptr(static_scale),
                                         _ptr(q_out), _ptr(scale_out), _stream(stream)),
           "vqlin_act_hadamard_quant")
+    return q_out, scale_out
+
+
+def act_adaln_hadamard_quant(X, bits: int, hadamard_block: int, ada_scale, ada_shift, eps: float = 1e-6,
+                             static_scale=None, q_out=None, scale_out=None, stream=None):
+    """AdaLayerNorm of X [M, K] bf16 (per token, then (1 + ada_scale) and
+    ada_shift per channel), rotated block-wise and quantized per token, in one
+    kernel.  Returns (q, s) in the encoding of act_hadamard_quant."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(ada_scale, "ada_scale", torch.float32, 1)
+    _need(ada_shift, "ada_shift", torch.float32, 1)
+    M, K = X.shape
+    if q_out is None:
+        q_out = torch.empty((M, K), dtype=torch.uint8 if bits == 4 else torch.int16, device=X.device)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=X.device)
+    if static_scale is not None:
+        _need(static_scale, "static_scale", torch.float32)
+    check(_lib.vqlin_act_adaln_hadamard_quant(_ptr(X), M, K, bits, hadamard_block, _ptr(ada_scale), _ptr(ada_shift),
+                                              float(eps), _ptr(static_scale), _ptr(q_out), _ptr(scale_out),
+                                              _stream(stream)),
+          "vqlin_act_adaln_hadamard_quant")
     return q_out, scale_out
 
 

@@ -16,7 +16,11 @@
 //     shared memory across warps); one CTA holds one or more whole tokens;
 //   * optional channel scaling (FoldQuantVLA abstract: channel scaling
 //     combined with the block Hadamard transform): x' = x / c per input
-//     channel, an IEEE division of each loaded value, before the rotation.
+//     channel, an IEEE division of each loaded value, before the rotation;
+//   * optional AdaLayerNorm before the rotation (Omega-QVLA summary: the QKV
+//     projections follow an AdaLayerNorm): the token's mean and population
+//     variance from its registers, then (x - mean)/sqrt(var + eps) * (1 +
+//     scale[k]) + shift[k], kept in float32 (never rounded to bf16).
 #include "act_codes.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -33,10 +37,11 @@ struct BlockGeom {
   static constexpr int G = 32 * LPG;                   // channels per lane group
 };
 
-template <int BITS, int HB, int UPT>
+template <int BITS, int HB, int UPT, bool ADA>
 __global__ void __launch_bounds__(512)
 act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
                  const float* __restrict__ static_scale, const float* __restrict__ chan,
+                 const float* __restrict__ ada_scale, const float* __restrict__ ada_shift, float eps,
                  uint8_t* __restrict__ Q, float* __restrict__ S) {
   using Geo = BlockGeom<HB>;
   constexpr int LPG = Geo::LPG, G = Geo::G;
@@ -78,11 +83,87 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
         for (int e = 0; e < 8; ++e) v[i][j][e] = __fdiv_rn(v[i][j][e], c[e]);
       }
     }
-    if (HB > 0) hadamard_unit<HB == 0 ? 128 : HB>(v[i], lane);
+    if (!ADA) {  // without the normalisation, rotate while the next unit's loads are in flight
+      if (HB > 0) hadamard_unit<HB == 0 ? 128 : HB>(v[i], lane);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][j][e]));
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][j][e]));
+    }
+  }
+
+  // the token's sum over its tpr threads in a fixed order (shuffle tree, then
+  // the warps' partials in warp order); every thread of the CTA calls it
+  auto token_sum = [&](float x) -> float {
+    if (tpr <= 32) {
+      for (int o = tpr >> 1; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      return x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    __syncthreads();  // red may still be read by the previous reduction
+    if (lane == 0) red[threadIdx.x >> 5] = x;
+    __syncthreads();
+    const int wpr = tpr >> 5, w0 = r * wpr;
+    float t = 0.0f;
+    if (r < rpc)
+      for (int w = 0; w < wpr; ++w) t += red[w0 + w];
+    return t;
+  };
+
+  if constexpr (ADA) {
+    // AdaLayerNorm of the token before its rotation (the normalisation fused
+    // into this kernel): (x - mean) / sqrt(var + eps) * (1 + scale) + shift,
+    // mean and population variance over the K channels in float32 (two
+    // passes over the registers)
+    float s1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < UPT; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s1 += v[i][j][e];
+    const float mean = __fdiv_rn(token_sum(s1), (float)K);
+    float s2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      const bool ok = row_ok && ut + i * tpr < units;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = ok ? v[i][j][e] - mean : 0.0f;
+          s2 = fmaf(d, d, s2);
+        }
+    }
+    const float var = __fdiv_rn(token_sum(s2), (float)K);
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(var + eps));
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      const int u = ut + i * tpr;
+      if (!(row_ok && u < units)) continue;
+      const int g = u / LPG, l = u % LPG;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const size_t ch = (size_t)g * G + (l + LPG * j) * 8;
+        const float4 a0 = __ldg(reinterpret_cast<const float4*>(ada_scale + ch));
+        const float4 a1 = __ldg(reinterpret_cast<const float4*>(ada_scale + ch + 4));
+        const float4 b0 = __ldg(reinterpret_cast<const float4*>(ada_shift + ch));
+        const float4 b1 = __ldg(reinterpret_cast<const float4*>(ada_shift + ch + 4));
+        const float sc[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float sh[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][j][e] = fmaf((v[i][j][e] - mean) * rstd, 1.0f + sc[e], sh[e]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+      if (HB > 0) hadamard_unit<HB == 0 ? 128 : HB>(v[i], lane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[i][j][e]));
+    }
   }
 
   float s;
@@ -95,6 +176,7 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
     } else {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (ADA) __syncthreads();  // the normalisation's sums may still be read from red
       if (lane == 0) red[threadIdx.x >> 5] = amax;
       __syncthreads();
       const int wpr = tpr >> 5, w0 = r * wpr;
@@ -133,8 +215,8 @@ act_quant_kernel(const uint16_t* __restrict__ X, int M, int K, int tpr, int rpc,
 }
 
 template <int BITS, int HB>
-cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, const float* chan, void* q, float* s,
-                      cudaStream_t st) {
+cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, const float* chan, const float* ada_scale,
+                      const float* ada_shift, float eps, void* q, float* s, cudaStream_t st) {
   const int units = K / 32;
   const int upt = units <= 512 ? 1 : (units <= 1024 ? 2 : 4);  // at most 512 threads per token
   int tpr = (units + upt - 1) / upt;
@@ -159,9 +241,24 @@ cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, const fl
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   uint8_t* qb = static_cast<uint8_t*>(q);
-  if (upt == 1) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1>, X, M, K, tpr, rpc, ss, chan, qb, s);
-  if (upt == 2) return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2>, X, M, K, tpr, rpc, ss, chan, qb, s);
-  return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4>, X, M, K, tpr, rpc, ss, chan, qb, s);
+  if (ada_scale != nullptr) {
+    if (upt == 1)
+      return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1, true>, X, M, K, tpr, rpc, ss, chan, ada_scale,
+                                ada_shift, eps, qb, s);
+    if (upt == 2)
+      return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2, true>, X, M, K, tpr, rpc, ss, chan, ada_scale,
+                                ada_shift, eps, qb, s);
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4, true>, X, M, K, tpr, rpc, ss, chan, ada_scale,
+                              ada_shift, eps, qb, s);
+  }
+  if (upt == 1)
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 1, false>, X, M, K, tpr, rpc, ss, chan, nullptr,
+                              nullptr, 0.0f, qb, s);
+  if (upt == 2)
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 2, false>, X, M, K, tpr, rpc, ss, chan, nullptr,
+                              nullptr, 0.0f, qb, s);
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel<BITS, HB, 4, false>, X, M, K, tpr, rpc, ss, chan, nullptr,
+                            nullptr, 0.0f, qb, s);
 }
 
 }  // namespace
@@ -169,16 +266,17 @@ cudaError_t launch_hb(const uint16_t* X, int M, int K, const float* ss, const fl
 namespace vqlin {
 
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
-                             const float* static_scale, void* q, float* s, cudaStream_t st, const float* chan) {
+                             const float* static_scale, void* q, float* s, cudaStream_t st, const float* chan,
+                             const float* ada_scale, const float* ada_shift, float eps) {
   if (M == 0) return cudaSuccess;
   if (bits == 4) {
-    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, chan, q, s, st);
-    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, chan, q, s, st);
-    return launch_hb<4, 128>(X, M, K, static_scale, chan, q, s, st);
+    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    return launch_hb<4, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
   }
-  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, chan, q, s, st);
-  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, chan, q, s, st);
-  return launch_hb<8, 128>(X, M, K, static_scale, chan, q, s, st);
+  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+  return launch_hb<8, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
 }
 
 }  // namespace vqlin

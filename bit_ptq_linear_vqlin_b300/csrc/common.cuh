@@ -47,7 +47,8 @@ int max_active_clusters(const void* kernel, int threads, size_t dyn_smem, int cl
 // for weights W * c), null for none
 cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
                              const float* static_scale, void* q, float* s, cudaStream_t st,
-                             const float* chan = nullptr);
+                             const float* chan = nullptr, const float* ada_scale = nullptr,
+                             const float* ada_shift = nullptr, float eps = 0.0f);
 cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, int hb,
                                     void* q, float* s, cudaStream_t st, const float* chan = nullptr);
 cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,

@@ -355,6 +355,28 @@ vqlin_status vqlin_debug_gemm_withheld_loads(int bits, const void* xq, const voi
                                          static_cast<cudaStream_t>(stream));
 }
 
+vqlin_status vqlin_act_adaln_hadamard_quant(const uint16_t* X, int M, int K, int bits, int hadamard_block,
+                                            const float* ada_scale, const float* ada_shift, float eps,
+                                            const float* static_scale, void* q_out, float* scale_out, void* stream) {
+  REQUIRE(M >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d K=%d", M, K);
+  REQUIRE(bits == 4 || bits == 8, VQLIN_ERR_INVALID_ARG, "bits must be 4 or 8 (got %d)", bits);
+  REQUIRE(hadamard_block == 0 || hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
+          "hadamard_block must be 0, 64 or 128 (got %d)", hadamard_block);
+  REQUIRE(K % 32 == 0, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 32", K);
+  REQUIRE(hadamard_block == 0 || K % hadamard_block == 0, VQLIN_ERR_UNSUPPORTED_SHAPE,
+          "K=%d is not a multiple of the Hadamard block %d", K, hadamard_block);
+  REQUIRE(K <= vqlin::kActQuantMaxK, VQLIN_ERR_UNSUPPORTED_SHAPE, "K=%d exceeds %d", K, vqlin::kActQuantMaxK);
+  REQUIRE(eps >= 0.0f && eps == eps, VQLIN_ERR_INVALID_ARG, "eps must be a non-negative number");
+  if (M == 0) return VQLIN_OK;
+  REQUIRE_PTR(X); REQUIRE_PTR(ada_scale); REQUIRE_PTR(ada_shift); REQUIRE_PTR(q_out); REQUIRE_PTR(scale_out);
+  REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(ada_scale); REQUIRE_ALIGNED(ada_shift); REQUIRE_ALIGNED(q_out);
+  REQUIRE((reinterpret_cast<uintptr_t>(scale_out) & 3) == 0, VQLIN_ERR_MISALIGNED, "scale_out is not 4-byte aligned");
+  return vqlin::check_launch(vqlin::launch_act_quant(X, M, K, bits, hadamard_block, static_scale, q_out, scale_out,
+                                                     static_cast<cudaStream_t>(stream), nullptr, ada_scale, ada_shift,
+                                                     eps),
+                             "act_adaln_hadamard_quant");
+}
+
 vqlin_status vqlin_composite_rotation_prepare(const uint16_t* W, int N, int K, int block, int32_t* perm_out,
                                               double* R_out, void* stream) {
   REQUIRE(N > 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes N=%d K=%d", N, K);

@@ -313,6 +313,23 @@ vqlin_status vqlin_act_hadamard_quant_scaled(const uint16_t* X, int M, int K, in
                                              float* scale_out, void* stream);
 
 /*
+ * The normalisation before the projection fused into the activation kernel
+ * (Omega-QVLA technical summary, "Scalatura delle Attivazioni DiT per Passo":
+ * the QKV projections follow an AdaLayerNorm).  Per token:
+ *   x^ = (x - mean) / sqrt(var + eps)   (mean and population variance over
+ *        the K channels, float32, no learned affine part),
+ *   y  = x^ * (1 + ada_scale[k]) + ada_shift[k]   (the conditioning's
+ *        modulation, one K-vector pair for every token of the call),
+ * then exactly vqlin_act_hadamard_quant of y (rotation by blockdiag(H_b /
+ * sqrt(b)), dynamic or static per-token quantization); y stays in float32 and
+ * is never rounded to bf16.  ada_scale, ada_shift: float [K] on the device,
+ * 16-byte aligned; eps >= 0.  Other arguments as vqlin_act_hadamard_quant.
+ */
+vqlin_status vqlin_act_adaln_hadamard_quant(const uint16_t* X, int M, int K, int bits, int hadamard_block,
+                                            const float* ada_scale, const float* ada_shift, float eps,
+                                            const float* static_scale, void* q_out, float* scale_out, void* stream);
+
+/*
  * Composite SVD . Hadamard block rotation with a zig-zag channel permutation
  * (Omega-QVLA technical summary, "Rotazione Composita SVD.Hadamard": "Rotazione
  * SVD", "Rotazione Hadamard", "Implementazione a Blocchi").  Three calls:

@@ -99,6 +99,12 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_bf16_ref(A, A, None, A, 4, 12, 256, None) == UNSUPPORTED
     assert lib.vqlin_debug_gemm_s32(5, A, A, A, 4, 4, 256, None) == INVALID
     assert lib.vqlin_debug_gemm_s32(4, A, A, None, 4, 4, 256, None) == INVALID
+    f = lib.vqlin_act_adaln_hadamard_quant
+    assert f(A, 16, 256, 4, 128, None, A, 1e-6, None, A, A, None) == INVALID      # null scale vector
+    assert f(A, 16, 256, 4, 128, A, A, -1.0, None, A, A, None) == INVALID         # eps < 0
+    assert f(A, 16, 192, 4, 128, A, A, 1e-6, None, A, A, None) == UNSUPPORTED     # K % b
+    assert f(A, 16, 256, 4, 128, A + 4, A, 1e-6, None, A, A, None) == MISALIGNED
+    assert f(A, 0, 256, 8, 64, A, A, 1e-6, None, A, A, None) == OK               # empty: no-op
     f = lib.vqlin_composite_rotation_prepare
     assert f(A, 16, 256, 32, A, A, None) == INVALID          # block size
     assert f(A, 16, 192, 128, A, A, None) == UNSUPPORTED     # K % b
