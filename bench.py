@@ -387,7 +387,6 @@ class ControlStepStack:
                              y4=torch.empty((self.M_exp, g["N"]), dtype=torch.bfloat16, device=dev),
                              y16=torch.empty((self.M_exp, g["N"]), dtype=torch.bfloat16, device=dev))
                         for g in self.exp_groups]
-        self.launches_per_step = 0
         self.instrument = None  # callable(key, fn) while capturing an instrumented graph
 
     # -- launch helpers -------------------------------------------------------
@@ -396,7 +395,6 @@ class ControlStepStack:
             fn()
         else:
             self.instrument(key, fn)
-        self.launches_per_step += 1
 
     def prefix(self):
         vq = self.vq
@@ -540,13 +538,18 @@ def read_traffic(kernel_key):
         fields = dict(kv.split("=", 1) for kv in ln[len("traffic "):].split(";") if "=" in kv)
         if fields.get("key") != key:
             continue
-        src = os.path.join(ROOT, fields.get("source", ""))
-        try:
-            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        except OSError:
+        # a class of two kernels (activation kernel + codes GEMM) lists both sources
+        srcs = fields.get("source", "").split(",")
+        shas = fields.get("sha", "").split(",")
+        if len(srcs) != len(shas):
             return None
-        if sha != fields.get("sha"):
-            return None  # the kernel changed since the counters were taken
+        for src, want in zip(srcs, shas):
+            try:
+                sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+            except OSError:
+                return None
+            if sha != want:
+                return None  # a kernel changed since the counters were taken
         return float(fields["bytes"])
     return None
 
@@ -571,10 +574,16 @@ def run_vqlin(args):
 
     # the step as three CUDA graphs (prefix, expert at W4A4, expert at W4A16)
     graphs = [capture(torch, part) for part in (stack.prefix, stack.expert_w4a4, stack.expert_w4a16)]
-    stack.launches_per_step = 0
-    full_step()  # count launches of one step (eager, untimed)
+    # count the library's kernel launches of one step (eager, untimed); a call
+    # may launch more than one kernel (activation kernel + codes GEMM)
+    n0 = stack.vq.kernel_launch_count()
+    full_step()
     torch.cuda.synchronize()
-    launches_per_step = stack.launches_per_step
+    launches_per_step = stack.vq.kernel_launch_count() - n0
+    # launches the GPU ran before the first warm-up step (the captures recorded
+    # one step's worth without running it): the skip count of a launch list
+    print(f"library kernel launches run before the first warm-up step: "
+          f"{stack.vq.kernel_launch_count() - launches_per_step}", file=sys.stderr)
 
     def step():
         for g in graphs:
@@ -714,6 +723,9 @@ def run_vqlin(args):
                      f"({'kind::f8f6f4 e4m3' if kind_peak == 'e4m3' else 'kind::f16 bf16'}), measured in this run")
     traffic = read_traffic(dom)
 
+    # -- fixed cost of a dependent launch per kernel class (rank 0)
+    floor = launch_floor(torch, stack.vq, dev) if rank == 0 and not args.skip_shapes else None
+
     # -- per-shape lines of configs 1-4 (rank 0)
     shapes = None
     if rank == 0 and not args.skip_shapes:
@@ -755,6 +767,7 @@ def run_vqlin(args):
             "e2e": {"value": world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clock_info,
+            "launch_floor_us": floor,
             "parts_ms": part_ms,
             "bf16_cublas_ms": bf16_ms,
             "kernel_share_ms_per_step": {" ".join(str(x) for x in k): round(v[0], 4)
@@ -1024,6 +1037,38 @@ def per_shape_lines(torch, vq, dev, seed, tensor_peaks, hbm_gbs):
             lines.append(e)
             torch.cuda.empty_cache()
     return lines
+
+
+def launch_floor(torch, vq, dev, n=180):
+    """Per-launch time of n dependent launches of the smallest case of each
+    kernel class (one CUDA graph, programmatic dependent launch as in the
+    step): the fixed cost a few-token projection pays before its own work."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    T = ShapeTimer(torch, dev)
+
+    def bf16(r, c):
+        return torch.randn((r, c), generator=g, device=dev).to(torch.bfloat16)
+
+    M, N, K = 16, 128, 128
+    X, Xs, W = bf16(M, K), bf16(1, K), bf16(N, K)
+    wq, sw = vq.quantize_weights_rtn(W, 4, True, 0, 128)
+    q16, s16, z16 = vq.quantize_weights_rtn(W, 4, False, 128, 0)
+    st = torch.full((1,), 0.5, device=dev)
+    xq1 = torch.empty((1, K), dtype=torch.uint8, device=dev)
+    sx1 = torch.empty(1, device=dev)
+    xq, sx = vq.act_hadamard_quant(X, 4, 128)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    xqs = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    cases = {
+        "act_quant 1x128": lambda: vq.act_hadamard_quant(Xs, 4, 128, q_out=xq1, scale_out=sx1),
+        "linear_w4a4 16x128x128 (codes)": lambda: vq.linear_w4a4(xq, sx, wq, sw, out=y),
+        "linear_w4a4_static 16x128x128 (one launch)":
+            lambda: vq.linear_w4a4_static(X, st, wq, sw, 128, out=y, xq_out=xqs),
+        "linear_w4a16 16x128x128": lambda: vq.linear_w4a16(X, q16, s16, z16, 128, out=y),
+        "cuBLAS bf16 16x128x128": lambda: vq.linear_bf16_ref(X, W, out=y),
+    }
+    return {k: round(min(T.time([f] * n, reps=4) for _ in range(3)), 3) for k, f in cases.items()}
 
 
 def measure_tensor_peaks(vq):

@@ -31,7 +31,7 @@ __all__ = [
     "linear_w4a8", "linear_w4a16", "linear_bf16_ref", "debug_gemm_s32", "debug_gemm_w4a8_s32",
     "debug_gemm_withheld_loads", "debug_w4a16_withheld_loads", "measure_mma_rate",
     "composite_rotation_prepare", "quantize_weights_composite", "act_composite_quant",
-    "init", "shutdown", "act_adaln_hadamard_quant",
+    "init", "shutdown", "kernel_launch_count", "act_adaln_hadamard_quant",
     "get_last_device_error",
 ]
 
@@ -69,6 +69,13 @@ def init() -> None:
 def shutdown() -> None:
     """Release the library's per-device state (after each device's queued work)."""
     check(_lib.vqlin_shutdown(), "vqlin_shutdown")
+
+
+def kernel_launch_count() -> int:
+    """The library's own kernel launches since it was loaded (graph replays not included)."""
+    n = ctypes.c_ulonglong(0)
+    check(_lib.vqlin_kernel_launch_count(ctypes.byref(n)), "vqlin_kernel_launch_count")
+    return int(n.value)
 
 
 def get_last_device_error(stream=None) -> None:

@@ -44,6 +44,7 @@ SIGNATURES = {
     "vqlin_debug_w4a16_withheld_loads": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, ctypes.c_uint64, _p]),
     "vqlin_composite_rotation_prepare": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "vqlin_act_adaln_hadamard_quant": (_i, [_p, _i, _i, _i, _i, _p, _p, ctypes.c_float, _p, _p, _p, _p]),
+    "vqlin_kernel_launch_count": (_i, [_p]),
     "vqlin_init": (_i, []),
     "vqlin_shutdown": (_i, []),
     "vqlin_quantize_weights_rtn_scaled": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p]),

@@ -269,14 +269,17 @@ cudaError_t launch_act_quant(const uint16_t* X, int M, int K, int bits, int hb,
                              const float* static_scale, void* q, float* s, cudaStream_t st, const float* chan,
                              const float* ada_scale, const float* ada_shift, float eps) {
   if (M == 0) return cudaSuccess;
+  cudaError_t e;
   if (bits == 4) {
-    if (hb == 0) return launch_hb<4, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
-    if (hb == 64) return launch_hb<4, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
-    return launch_hb<4, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    if (hb == 0) e = launch_hb<4, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    else if (hb == 64) e = launch_hb<4, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    else e = launch_hb<4, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+  } else {
+    if (hb == 0) e = launch_hb<8, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    else if (hb == 64) e = launch_hb<8, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+    else e = launch_hb<8, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
   }
-  if (hb == 0) return launch_hb<8, 0>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
-  if (hb == 64) return launch_hb<8, 64>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
-  return launch_hb<8, 128>(X, M, K, static_scale, chan, ada_scale, ada_shift, eps, q, s, st);
+  return launched(e);
 }
 
 }  // namespace vqlin

@@ -15,6 +15,10 @@ namespace vqlin {
 // Records a detail message for vqlin_last_error_message() and returns `st`.
 vqlin_status fail(vqlin_status st, const char* fmt, ...);
 
+// Host-side tally of the library's kernel launches: adds n to the count
+// that vqlin_kernel_launch_count() reports when e is cudaSuccess; returns e.
+cudaError_t launched(cudaError_t e, int n = 1);
+
 // Address of the per-device status word (a __device__ int), for kernels that
 // report bounded-wait timeouts.  Never null after a successful call.
 int* device_status_word();

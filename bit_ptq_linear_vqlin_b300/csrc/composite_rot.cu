@@ -452,7 +452,7 @@ cudaError_t prepare_b(const uint16_t* W, int N, int K, int* perm, double* R, int
   cudaError_t e = set_smem_once<&jacobi_kernel<B>>(jacobi_smem<B>());
   if (e != cudaSuccess) return e;
   jacobi_kernel<B><<<K / B, kThreads, jacobi_smem<B>(), st>>>(R, status);
-  return cudaGetLastError();
+  return vqlin::launched(cudaGetLastError(), 4);
 }
 
 template <typename T, int B, int BITS, bool WEIGHT>
@@ -469,7 +469,7 @@ cudaError_t rotate_quant_b(const uint16_t* X, int rows, int K, const int* perm, 
   rotate_rows_kernel<T, B, BITS, WEIGHT, 0><<<grid, kThreads, smem, st>>>(X, rows, K, perm, R, amax, Q);
   rotate_rows_kernel<T, B, BITS, WEIGHT, 1><<<grid, kThreads, smem, st>>>(X, rows, K, perm, R, amax, Q);
   finalize_scale_kernel<BITS><<<(rows + 255) / 256, 256, 0, st>>>(amax, rows);
-  return cudaGetLastError();
+  return vqlin::launched(cudaGetLastError(), 3);
 }
 
 template <typename T, bool WEIGHT>

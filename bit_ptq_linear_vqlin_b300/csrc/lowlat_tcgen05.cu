@@ -640,7 +640,7 @@ vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const u
   attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a4_lowlat_kernel<FUSED, HB>, tmW, tmXq, a);
+  const cudaError_t e = vqlin::launched(cudaLaunchKernelEx(&cfg, w4a4_lowlat_kernel<FUSED, HB>, tmW, tmXq, a));
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a4 low-latency launch (grid %d x %d x %d, cluster %d x %d, %zu B): %s",
                        p.tiles_n_pad, p.tiles_m, p.S, p.cn, p.S, p.dyn, cudaGetErrorString(e));

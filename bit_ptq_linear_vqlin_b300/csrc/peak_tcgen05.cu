@@ -146,6 +146,7 @@ extern "C" vqlin_status vqlin_measure_mma_rate(int kind, int a_in_tmem, int n, i
       out = vqlin::fail(VQLIN_ERR_CUDA, "measure_mma_rate: %s", cudaGetErrorString(e));
       break;
     }
+    vqlin::launched(e, 2);
     float ms = 0.0f;
     cudaEventElapsedTime(&ms, a, b);
     const int kdim = kind == 0 ? 32 : 16;  // K of one MMA

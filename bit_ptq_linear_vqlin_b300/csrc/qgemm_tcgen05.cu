@@ -978,7 +978,7 @@ vqlin_status launch_bits(const void* xq, const float* sx, const void* wq, const 
   attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmW, tmX, tmY, a);
+  const cudaError_t e = vqlin::launched(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, tmY, a));
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "qgemm launch (grid %d x %d x %d, cluster %d, %zu B smem): %s", tiles_n,
                        tiles_m, S, S, cfg.dynamicSmemBytes, cudaGetErrorString(e));

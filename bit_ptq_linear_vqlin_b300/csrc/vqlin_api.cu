@@ -5,6 +5,7 @@
 // memory the library owns is the cuBLASLt workspace of the bf16 baseline,
 // created once per device by vqlin_init() or on first use, and released by
 // vqlin_shutdown().
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <map>
@@ -80,12 +81,27 @@ vqlin_status fail(vqlin_status st, const char* fmt, ...) {
   return st;
 }
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+cudaError_t launched(cudaError_t e, int n) {
+  if (e == cudaSuccess) g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed);
+  return e;
+}
+
 int* device_status_word() {
   DeviceState* s = nullptr;
   return device_state(&s, false) == VQLIN_OK ? s->status_word : nullptr;
 }
 
 }  // namespace vqlin
+
+extern "C" vqlin_status vqlin_kernel_launch_count(unsigned long long* count) {
+  if (count == nullptr) return vqlin::fail(VQLIN_ERR_INVALID_ARG, "vqlin_kernel_launch_count: count is null");
+  *count = vqlin::g_launches.load(std::memory_order_relaxed);
+  return VQLIN_OK;
+}
 
 extern "C" vqlin_status vqlin_init(void) {
   vqlin::DeviceState* s = nullptr;

@@ -449,10 +449,10 @@ cudaError_t launch_w4a16_gemv(const uint16_t* X, const uint8_t* wq, const uint16
   // more than it saves (6.8 -> 7.5 us).  With two or four tokens that
   // variant's registers spill at 512 threads, so those keep the other one.
   if (mt == 1 && (long long)N * K >= (32ll << 20) && (size_t)K * 4 + (size_t)(K / 32) * 4 <= kMaxXSmem)
-    return launch_smem<1>(X, wq, s, z, group, bias, Y, M, N, K, st);
-  if (mt == 1) return launch_mt<1>(X, wq, s, z, group, bias, Y, M, N, K, st);
-  if (mt == 2) return launch_mt<2>(X, wq, s, z, group, bias, Y, M, N, K, st);
-  return launch_mt<4>(X, wq, s, z, group, bias, Y, M, N, K, st);  // M <= kW4a16GemvMaxM
+    return launched(launch_smem<1>(X, wq, s, z, group, bias, Y, M, N, K, st));
+  if (mt == 1) return launched(launch_mt<1>(X, wq, s, z, group, bias, Y, M, N, K, st));
+  if (mt == 2) return launched(launch_mt<2>(X, wq, s, z, group, bias, Y, M, N, K, st));
+  return launched(launch_mt<4>(X, wq, s, z, group, bias, Y, M, N, K, st));  // M <= kW4a16GemvMaxM
 }
 
 }  // namespace vqlin

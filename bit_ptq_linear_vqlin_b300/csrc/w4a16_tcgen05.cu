@@ -588,7 +588,7 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BT, GROUP>, tmW, tmX, a);
+  const cudaError_t e = vqlin::launched(cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BT, GROUP>, tmW, tmX, a));
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a16 launch (grid %d x %d x %d, %zu B smem): %s", tiles_n, tiles_m, S,
                        cfg.dynamicSmemBytes, cudaGetErrorString(e));

@@ -179,7 +179,7 @@ cudaError_t launch_weight_quant_sym(const uint16_t* W, int N, int K, int bits, i
     if (e != cudaSuccess) return e;
     weight_quant_sym_kernel<8><<<N, kSymThreads, smem, st>>>(W, K, hb, chan, (uint8_t*)q, s);
   }
-  return cudaGetLastError();
+  return launched(cudaGetLastError());
 }
 
 cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group, uint8_t* q,
@@ -192,7 +192,7 @@ cudaError_t launch_weight_quant_asym(const uint16_t* W, int N, int K, int group,
     case 128: weight_quant_asym_kernel<4><<<grid, 256, 0, st>>>(W, N, K, q, s, z); break;
     default: weight_quant_asym_kernel<8><<<grid, 256, 0, st>>>(W, N, K, q, s, z); break;
   }
-  return cudaGetLastError();
+  return launched(cudaGetLastError());
 }
 
 }  // namespace vqlin

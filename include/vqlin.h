@@ -100,6 +100,15 @@ vqlin_status vqlin_init(void);
 vqlin_status vqlin_shutdown(void);
 
 /*
+ * Number of the library's own kernels launched (enqueued on a stream or
+ * recorded into a CUDA graph being captured) since the library was loaded,
+ * over all devices and threads.  A graph replay launches nothing through the
+ * library and is not counted.  count: host pointer; VQLIN_ERR_INVALID_ARG if
+ * null.  The pages define no such call.
+ */
+vqlin_status vqlin_kernel_launch_count(unsigned long long* count);
+
+/*
  * Offline weight preparation: round-to-nearest quantization of W [N, K] bf16.
  * ("plain RTN", LoopQ abstract; rotation folded into the weights,
  * FoldQuantVLA abstract and Omega-QVLA "Rotazione Hadamard".)

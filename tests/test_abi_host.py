@@ -75,6 +75,17 @@ def test_shutdown_without_state_is_a_no_op(lib):
     assert lib.vqlin_shutdown() == OK
 
 
+def test_launch_count_is_host_side(lib):
+    # the tally needs no device; rejected calls (no device, bad arguments) launch nothing
+    import ctypes
+    n = ctypes.c_ulonglong(12345)
+    assert lib.vqlin_kernel_launch_count(ctypes.byref(n)) == OK
+    before = n.value
+    assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED
+    assert lib.vqlin_kernel_launch_count(ctypes.byref(n)) == OK and n.value == before
+    assert lib.vqlin_kernel_launch_count(None) == INVALID
+
+
 def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED
     assert lib.vqlin_linear_w8a8(A, A, A, A, None, A, 16, 16, 96, None) == UNSUPPORTED
