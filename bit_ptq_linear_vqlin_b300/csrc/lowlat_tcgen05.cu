@@ -310,10 +310,16 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         fence_proxy_async_global();
         load_codes();
       }
-      // copies in flight complete before the CTA may exit
-      for (int j = 0; j < cnt; ++j) {
-        if (!mbar_wait_bounded(&wfull[j], 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
-        if (!mbar_wait_bounded(&bfull[j], 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
+      // copies in flight complete before the CTA may exit: once every MMA
+      // has completed, every copy has landed; only a CTA that gave up checks
+      // them one by one.  (Checking the 2 x cnt barriers in turn kept this
+      // warp from the final barrier ~1.5 us after the MMAs had finished.)
+      const bool all_done = mbar_wait_bounded(acc_full, 0, a.wait_limit_ns, abort);
+      if (!all_done || *abort) {
+        for (int j = 0; j < cnt; ++j) {
+          if (!mbar_wait_bounded(&wfull[j], 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
+          if (!mbar_wait_bounded(&bfull[j], 0, a.wait_limit_ns, nullptr)) record_timeout(a.status, abort);
+        }
       }
     }
   } else if (warp == 1) {
@@ -407,11 +413,15 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
   };
 
   if (S == 1) {
-    // straight from tensor memory to global memory: thread = channel, 16
-    // tokens per load; for each token a warp writes 32 consecutive channels
+    // thread = channel, 16 tokens per tensor-memory load; each warp stages its
+    // 16 tokens x 32 channels as bf16 over the dead operand tiles and writes
+    // every token's 64 bytes as four 16-byte stores (a warp's 2-byte stores
+    // to 16 token rows measured ~35 ns each)
     if (go) {
       const int n = n0 + row;
       const float sw_n = s_sw[row], b_n = s_bias[row];
+      const bool vec = (a.N & 7) == 0;  // 16-byte aligned token rows
+      uint16_t* stg = reinterpret_cast<uint16_t*>(base) + (warp - 2) * 512;
       for (int c0 = cfirst; c0 < bt; c0 += 32) {
         float f[16];
         load_sum(c0, f);
@@ -426,7 +436,20 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         uint16_t yb[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) yb[jj] = f32_to_bf16_rn(fmaf(f[jj] * sx[jj], sw_n, b_n));
-        if (n < a.N) {
+        if (vec) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) stg[jj * 32 + lane] = yb[jj];
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tok = h * 8 + (lane >> 2), part = lane & 3;
+            const int nn = n0 + q * 32 + part * 8;
+            if (c0 + tok < mt && nn < a.N)
+              *reinterpret_cast<uint4*>(a.Y + (size_t)(m0 + c0 + tok) * a.N + nn) =
+                  *reinterpret_cast<const uint4*>(stg + tok * 32 + part * 8);
+          }
+          __syncwarp();
+        } else if (n < a.N) {
           uint16_t* yp = a.Y + (size_t)(m0 + c0) * a.N + n;
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
