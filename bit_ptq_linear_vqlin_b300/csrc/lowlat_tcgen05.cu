@@ -132,7 +132,6 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
   uint64_t* bfull = s_bar + 2 * kMaxKb;    // [kMaxKb] activation codes landed
   uint64_t* acc_full = s_bar + 3 * kMaxKb; // every issuer's MMAs completed
   uint64_t* scl_ready = acc_full + 1;
-  uint64_t* red_full = acc_full + 2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)gridDim.z, split = (int)blockIdx.z;
@@ -164,7 +163,6 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
     mbar_init(acc_full, NI);
     mbar_init(scl_ready, 31);
-    mbar_init(red_full, 1);
     mbar_init_fence();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmXq);
@@ -460,19 +458,21 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_before();
     __syncthreads();
   } else {
-    // split K, reduce-scatter among the S CTAs of this output tile (cluster
-    // ranks cx + cn * r): split rank r owns channels [r rp, (r + 1) rp).
-    // Every CTA writes its int32 partial tile as S slices part[r][token][rp]
-    // over the dead operand tiles, then adds slice r into split rank r's slice
-    // with one bulk reduction; rank r scales and stores its slice once the
-    // S - 1 others have landed.  Integer sums: exact, in any order.
+    // split K among the S CTAs of this output tile (cluster ranks cx + cn *
+    // r): split rank r owns channels [r rp, (r + 1) rp).  Every CTA writes its
+    // int32 partial tile into its own shared memory as S slices
+    // part[r][token][rp] over the dead operand tiles; after one cluster
+    // barrier rank r reads slice r of every CTA of the tile (distributed
+    // shared memory, 16-byte loads), adds them, scales and stores; a second
+    // barrier keeps each CTA's shared memory alive until its peers have read
+    // it.  Integer sums: exact in any order.  (Pushing the slices with one
+    // bulk reduction per peer and waiting for them to land took 0.7 us more
+    // at 50 x 1024 x 4096.)
     const int rp = a.rows_per;
     const uint32_t slice_words = (uint32_t)(bt * rp);
-    const uint32_t slice_bytes = slice_words * 4u;
     const int own0 = split * rp;
     const int own_n = (live && own0 < kTileN) ? min(rp, kTileN - own0) : 0;
     uint32_t* part = reinterpret_cast<uint32_t*>(base);
-    if (tid == 64 && own_n > 0) mbar_arrive_expect_tx(red_full, (uint32_t)(S - 1) * slice_bytes);
     if (epi && live) {
       const int sl = row / rp, k = row - sl * rp;
       uint32_t* dst = part + (size_t)sl * slice_words + k;
@@ -482,7 +482,7 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
           load_sum(c0, f);
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) f[jj] = 0.0f;  // aborted: zeros, so every reduction completes
+          for (int jj = 0; jj < 16; ++jj) f[jj] = 0.0f;  // aborted: zeros (the status word reports it)
         }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -491,40 +491,29 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
           dst[(size_t)(c0 + jj) * rp] = (uint32_t)(__float_as_int(fmaf(f[jj], 262144.0f, 12582912.0f)) - 0x4B400000);
         }
       }
-      fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncwarp();
     cluster_sync_all();  // every CTA's partial slices are in place
-    const uint32_t part_s = smem_addr(part);
-    if (live && tid >= 64 && tid < 64 + S) {
-      const int r = tid - 64;
-      if (r != split && r * rp < kTileN) {
-        const uint32_t peer = (uint32_t)(cx + a.cn * r);
-        const uint32_t off = (uint32_t)r * slice_bytes;
-        bulk_reduce_add_u32_to_peer(mapa_shared(part_s + off, peer), part_s + off, slice_bytes,
-                                    mapa_shared(smem_addr(red_full), peer));
-      }
-    }
-    bool got = true;
-    if (own_n > 0) {
-      got = mbar_wait_bounded(red_full, 0, a.wait_limit_ns, nullptr);
-      if (!got) record_timeout(a.status, abort);
-    }
-    got = got && own_n > 0 && !*abort;
-    __syncwarp();
-    cluster_arrive();
-    if (got) {
+    if (own_n > 0 && !*abort) {
       const int nq = own_n / 4;
       const int total = nq * bt;
       const bool vec = (a.N & 3) == 0;
-      const uint32_t* mine = part + (size_t)split * slice_words;
+      const uint32_t mine = smem_addr(part + (size_t)split * slice_words);
       for (int idx = tid; idx < total; idx += kThreads) {
         const int c = idx / nq, k = 4 * (idx - c * nq);
         const int m = m0 + c, rr = own0 + k, n = n0 + rr;
         if (m >= a.M || n >= a.N) continue;
-        const uint4 t = *reinterpret_cast<const uint4*>(mine + (size_t)c * rp + k);
-        const int32_t acc[4] = {(int32_t)t.x, (int32_t)t.y, (int32_t)t.z, (int32_t)t.w};
+        const uint32_t src = mine + (uint32_t)((c * rp + k) * 4);
+        int32_t acc[4] = {0, 0, 0, 0};
+#pragma unroll 4
+        for (int r = 0; r < S; ++r) {
+          const float4 t = ld_shared_cluster_v4f(mapa_shared(src, (uint32_t)(cx + a.cn * r)));
+          acc[0] += __float_as_int(t.x);
+          acc[1] += __float_as_int(t.y);
+          acc[2] += __float_as_int(t.z);
+          acc[3] += __float_as_int(t.w);
+        }
         const float sx_m = s_sx[c];
         float y[4];
 #pragma unroll
@@ -538,7 +527,7 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
       }
     }
     __syncwarp();
-    cluster_wait();
+    cluster_sync_all();  // peers have read this CTA's slices
   }
   if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }

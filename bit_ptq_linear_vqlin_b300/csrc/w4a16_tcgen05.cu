@@ -227,10 +227,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           ph ^= 1u;
         }
       }
-      for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
-        if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr) ||
-            !mbar_wait_bounded(&fullx[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
-          record_timeout(a.status, abort);
+      // copies in flight complete before the CTA may exit: once every MMA
+      // has completed, every copy has landed; only a CTA that gave up checks
+      // the last ones one by one
+      const bool all_done = mbar_wait_bounded(done, 0, a.wait_limit_ns, abort);
+      if (!all_done || *abort) {
+        for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+          if (!mbar_wait_bounded(&full[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr) ||
+              !mbar_wait_bounded(&fullx[i % NS], (i / NS) & 1, a.wait_limit_ns, nullptr))
+            record_timeout(a.status, abort);
+      }
     }
   } else if (warp == 1 || (warp >= 14 && warp - 13 < a.issuers)) {
     // ------------------------------------------------------------ MMA issuers
@@ -296,7 +302,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // packed bytes, 64 channels), so one group's tensor-memory stores are in
     // flight while the other expands
     const int q = warp & 3, gr = (warp - 2) >> 2;
-    const int row = q * 32 + lane, n = n0 + row;
+    const int row = q * 32 + lane;
     const int sw = (row >> 2) & 1;  // 32-byte swizzle of the packed tile
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + a.a_col;
     // quantization group of this group's k-blocks: the next one differs by
