@@ -204,6 +204,9 @@ STATIC_CASES = [
     (50, 1024, 1024, 128), (50, 3072, 1024, 128), (50, 1024, 4096, 128), (50, 8192, 1024, 128),
     (1, 128, 128, 128), (16, 256, 256, 64), (33, 300, 2048, 64), (130, 264, 1024, 128), (816, 256, 2048, 128),
     (7, 1000, 16384, 128), (5, 256, 20480, 128), (64, 1160, 1024, 64), (50, 2056, 3072, 128),
+    # epilogue fallbacks: unsplit with N not a multiple of 8 (2-byte stores), split with N not a
+    # multiple of 4
+    (20, 300, 1024, 128), (24, 1030, 2048, 128),
 ]
 
 
@@ -432,6 +435,8 @@ LINEAR_CASES = [
     (816, 256, 2048, 128, "student_t4", 0.01, 30.0),
     (64, 512, 4096, 128, "normal", 0.005, 50.0),
     (17, 300, 11008, 128, "normal", 0.005, 50.0),
+    (40, 204, 1024, 128, "normal", 0.0, 1.0),          # few tokens, unsplit, N % 8 != 0
+    (9, 1030, 4096, 128, "normal", 0.0, 1.0),          # few tokens, split K, N % 4 != 0
 ]
 
 
