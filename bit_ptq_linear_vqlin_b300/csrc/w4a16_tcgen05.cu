@@ -500,8 +500,8 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
   // Among the splits whose clusters are all resident at once (one wave), the
   // one of least estimated time, a fit to launches timed on B300 at 8 to 64
   // tokens: ~1.7 us fixed, ~0.27 us per k-block of a CTA (its pipeline ring
-  // paces it), ~1 us for the cluster reduction when K is split, and ~0.02 us
-  // per CTA.  Splits other than powers of two (clusters of 3 or 6 CTAs timed
+  // paces it), ~1 us for the cluster reduction when K is split, and ~0.035 us
+  // per CTA (at 50 x 3072 x 1024 a split of 2 measured 5.03 us, of 4 5.44 us).  Splits other than powers of two (clusters of 3 or 6 CTAs timed
   // twice as slow) are left out unless the groups force one.  Without a
   // one-wave split, the smallest split.
   int S = 0, NS = 0, rows_per = 0, NI = 0;
@@ -552,7 +552,7 @@ vqlin_status launch_t(const uint16_t* X, const uint8_t* wq, const uint16_t* s, c
     const int active = vqlin::max_active_clusters((const void*)w4a16_tc_kernel<BT, GROUP>, kThreads, d, s_try);
     const bool wave = tiles_n * tiles_m <= active;
     const int ctas = tiles_n * tiles_m * s_try;
-    const double est = 1.7 + 0.27 * per_cta + (s_try > 1 ? 1.0 : 0.0) + 0.02 * ctas;
+    const double est = 1.7 + 0.27 * per_cta + (s_try > 1 ? 1.0 : 0.0) + 0.035 * ctas;
     const bool take = S == 0 || (wave && (!have_wave || est < best)) || (!wave && !have_wave && s_try < S);
     if (take) {
       S = s_try; NS = ns; a_col = ac; cols = c; dyn = d; NI = ni; ng_max = groups;

@@ -469,7 +469,7 @@ def test_linear_epilogue_with_oracle_codes(bits):
 
 
 @pytest.mark.parametrize("group", [64, 128, 256])
-@pytest.mark.parametrize("MNK", [(1, 4096, 4096), (4, 256, 1024), (5, 256, 1024), (50, 1024, 1024),
+@pytest.mark.parametrize("MNK", [(1, 4096, 4096), (4, 256, 1024), (5, 256, 1024), (50, 1024, 1024), (50, 3072, 1024),
                                  (50, 1024, 4096), (50, 8192, 1024), (64, 512, 11008), (7, 100, 256),
                                  (17, 300, 2048), (129, 264, 1024), (512, 384, 4096)])
 def test_linear_w4a16(group, MNK):
