@@ -30,7 +30,8 @@
 //   * codes variant: the codes come from the activation kernel; their TMA loads
 //     are issued right after the wait;
 //   * K longer than 8 k-blocks is split over the cluster's z dimension (at most
-//     16 CTAs per cluster) and reduced on chip as in the throughput GEMM.
+//     16 CTAs per cluster) and reduced on chip: each split rank reads its
+//     slice of every peer's int32 partial tile from distributed shared memory.
 // Roles (14 warps): warp 0 loads tiles (lane 0) and stages the epilogue's
 // scales (lanes 1..31); warps 2..9 expand the weights, then quantize
 // activations, then run the epilogue (two per tensor-memory lane quadrant);
