@@ -27,7 +27,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from oracle.vqlin_oracle import bf16_to_f64, block_hadamard_rotate, int_gemm, linear_epilogue, rtn_symmetric_rows
+from oracle.vqlin_oracle import (bf16_to_f64, block_hadamard_rotate, int_gemm, linear_epilogue, rtn_static,
+                                 rtn_symmetric_rows)
 
 
 def fold_output_scales(sw, factor) -> np.ndarray:
@@ -41,11 +42,14 @@ def head_factors(alpha, head_dim: int) -> np.ndarray:
 
 
 def linear_quantized_scaled(X_bits, W_bits, bits: int, hadamard_block: int, c=None, out_factor=None,
-                            bias_bits=None, act_bits=None):
+                            bias_bits=None, act_bits=None, static_scale=None):
     """Whole projection with channel scaling c (R25) and an output-scale fold
     (R24): W' = W diag(c) rotated offline and quantized per channel,
     x' = x diag(1/c) rotated online and quantized per token, integer GEMM,
-    epilogue with s_w' = s_w * f."""
+    epilogue with s_w' = s_w * f.  static_scale: one precomputed activation
+    scale for every token instead of the per-token scales (the per-step static
+    scales of the Omega-QVLA summary, "Scalatura delle Attivazioni DiT per
+    Passo"), codes clamped to the symmetric range."""
     W = bf16_to_f64(W_bits)
     X = bf16_to_f64(X_bits)
     if c is not None:
@@ -55,7 +59,12 @@ def linear_quantized_scaled(X_bits, W_bits, bits: int, hadamard_block: int, c=No
     Wt32 = block_hadamard_rotate(W, hadamard_block).astype(np.float32)
     wq, sw = rtn_symmetric_rows(Wt32, bits)
     Xt32 = block_hadamard_rotate(X, hadamard_block).astype(np.float32)
-    xq, sx = rtn_symmetric_rows(Xt32, bits if act_bits is None else act_bits)
+    abits = bits if act_bits is None else act_bits
+    if static_scale is None:
+        xq, sx = rtn_symmetric_rows(Xt32, abits)
+    else:
+        s = np.float32(static_scale)
+        xq, sx = rtn_static(Xt32, abits, s), np.full(Xt32.shape[0], s, dtype=np.float32)
     if out_factor is not None:
         sw = fold_output_scales(sw, out_factor)
     acc = int_gemm(xq, wq)

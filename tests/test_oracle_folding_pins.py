@@ -50,6 +50,23 @@ def test_channel_scaling_with_unit_factors_is_the_plain_projection():
     assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["acc"], b["acc"])
 
 
+def test_channel_scaling_with_a_static_scale():
+    # unit factors: the static-scale projection of the main oracle; and a
+    # static scale equal to every token's own dynamic scale gives the dynamic
+    # projection's codes
+    M, N, K = 8, 48, 256
+    xb, wb = activations(M, K, n_outliers=3, outlier_scale=20, seed=12), weights(N, K, seed=13)
+    s = o.calibrate_static_scale([xb], 4, 128)
+    a = sf.linear_quantized_scaled(xb, wb, 4, 128, c=np.ones(K), static_scale=s)
+    b = o.linear_quantized(xb, wb, 4, 128, static_scale=s)
+    assert np.array_equal(a["xq"], b["xq"]) and np.array_equal(a["y"], b["y"])
+    assert np.all(a["sx"] == np.float32(s))
+    c = np.exp(np.random.default_rng(14).normal(0, 0.3, K))
+    dyn = sf.linear_quantized_scaled(xb[:1], wb, 4, 128, c=c)
+    st = sf.linear_quantized_scaled(xb[:1], wb, 4, 128, c=c, static_scale=dyn["sx"][0])
+    assert np.array_equal(dyn["xq"], st["xq"]) and np.array_equal(dyn["y"], st["y"])
+
+
 def test_channel_scaling_moves_outlier_energy_into_the_weights():
     # dividing the outlier channels of x by c and multiplying W's columns by c
     # lowers the activation scale and raises the weight scales, the trade the
