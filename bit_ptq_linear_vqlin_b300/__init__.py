@@ -229,12 +229,13 @@ def linear_w4a4(xq, sx, wq, sw, bias=None, out=None, stream=None):
 
 
 def linear_w4a4_static(X, static_scale, wq, sw, hadamard_block: int = 128, bias=None, out=None,
-                       xq_out=None, stream=None):
+                       xq_out=None, stream=None, channel_scale=None):
     """W4A4 with the activations quantized inside the GEMM at a static scale:
     the same Y as act_hadamard_quant(X, 4, hadamard_block, static_scale) followed
     by linear_w4a4.  X bf16 [M, K], static_scale float32 (one element), wq uint8
     [N, K/2].  xq_out (uint8 [M, K], allocated if None) receives the activation
-    codes; the kernel also uses it to share them among its CTAs."""
+    codes; the kernel also uses it to share them among its CTAs.
+    channel_scale (float32 [K]): quantize X . diag(1/c) (wq from W . diag(c))."""
     _need(X, "X", torch.bfloat16, 2)
     _need(static_scale, "static_scale", torch.float32)
     _need(wq, "wq", torch.uint8, 2)
@@ -252,6 +253,13 @@ def linear_w4a4_static(X, static_scale, wq, sw, hadamard_block: int = 128, bias=
     _need(xq_out, "xq_out", torch.uint8, 2)
     if tuple(xq_out.shape) != (M, K):
         raise ValueError("xq_out must be [M, K]")
+    if channel_scale is not None:
+        _need(channel_scale, "channel_scale", torch.float32, 1)
+        check(_lib.vqlin_linear_w4a4_static_scaled(_ptr(X), _ptr(static_scale), _ptr(channel_scale), hadamard_block,
+                                                   _ptr(wq), _ptr(sw), _ptr(bias), _ptr(out), _ptr(xq_out), M, N, K,
+                                                   _stream(stream)),
+              "vqlin_linear_w4a4_static_scaled")
+        return out
     check(_lib.vqlin_linear_w4a4_static(_ptr(X), _ptr(static_scale), hadamard_block, _ptr(wq), _ptr(sw),
                                         _ptr(bias), _ptr(out), _ptr(xq_out), M, N, K, _stream(stream)),
           "vqlin_linear_w4a4_static")

@@ -33,6 +33,7 @@ SIGNATURES = {
     "vqlin_act_hadamard_quant": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p]),
     "vqlin_linear_w4a4": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w4a4_static": (_i, [_p, _p, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "vqlin_linear_w4a4_static_scaled": (_i, [_p, _p, _p, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w4a4_static_noalloc": (_i, [_p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w8a8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "vqlin_linear_w4a8": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _p]),

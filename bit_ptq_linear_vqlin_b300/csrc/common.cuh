@@ -102,9 +102,10 @@ constexpr int kLowlatMaxK = 16384;
 // Static-scale W4A4 whose activations are rotated and quantized on chip, once
 // per cluster, into the code buffer xq_ws [M, K] (bytes, the activation
 // kernel's encoding), which the CTAs then read back; any M, K <= kLowlatMaxK.
+// chan (optional, float [K]): channel scaling, x / c[k] before the rotation.
 vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_scale, int hb, uint8_t* xq_ws,
                                        const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
-                                       int N, int K, int* status, cudaStream_t st);
+                                       int N, int K, int* status, cudaStream_t st, const float* chan = nullptr);
 // The same kernel fed with the activation kernel's codes and per-token scales.
 // Whether the few-token W4A4 kernel's plan fits one wave of clusters.
 bool lowlat_one_wave(bool fused, int hb, int M, int N, int K);

@@ -67,6 +67,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct LowlatArgs {
   const uint16_t* X;            // FUSED: bf16 activations [M, K]
+  const float* chan;            // FUSED with CHAN: channel factors c [K] (x / c before the rotation)
   const float* static_scale;    // FUSED: one device float
   const float* sx;              // codes variant: per-token scales [M] (sx_step 1) or one scale (0)
   int sx_step;
@@ -113,7 +114,7 @@ __device__ __forceinline__ float ldg_nc_f32(const float* p) {
   return r;
 }
 
-template <bool FUSED, int HB>
+template <bool FUSED, int HB, bool CHAN = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXq,
                    const LowlatArgs a) {
@@ -209,6 +210,19 @@ w4a4_lowlat_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         v[c][2] = bf16_lo(raw[c].y); v[c][3] = bf16_hi(raw[c].y);
         v[c][4] = bf16_lo(raw[c].z); v[c][5] = bf16_hi(raw[c].z);
         v[c][6] = bf16_lo(raw[c].w); v[c][7] = bf16_hi(raw[c].w);
+      }
+      if (CHAN && ok) {
+        // channel scaling: x / c[k] by IEEE division before the rotation, as
+        // the activation kernel does
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float* cp = a.chan + (size_t)j * 128 + HB * g + 8 * (l + LPG * c);
+          const float4 c0 = __ldg(reinterpret_cast<const float4*>(cp));
+          const float4 c1 = __ldg(reinterpret_cast<const float4*>(cp + 4));
+          const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[c][e] = __fdiv_rn(v[c][e], cc[e]);
+        }
       }
       hadamard_unit<HB>(v, lane);
       if (ok) {
@@ -544,7 +558,7 @@ struct LowlatPlan {
   size_t dyn = 0;
 };
 
-template <bool FUSED, int HB>
+template <bool FUSED, int HB, bool CHAN = false>
 void set_attrs_once(cudaError_t* err) {
   // function attributes are per device: set them for every device used
   static std::mutex mu;
@@ -557,7 +571,7 @@ void set_attrs_once(cudaError_t* err) {
   }
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    const auto kern = w4a4_lowlat_kernel<FUSED, HB>;
+    const auto kern = w4a4_lowlat_kernel<FUSED, HB, CHAN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     res[dev] = e;
@@ -566,9 +580,9 @@ void set_attrs_once(cudaError_t* err) {
   *err = res[dev];
 }
 
-template <bool FUSED, int HB>
+template <bool FUSED, int HB, bool CHAN = false>
 bool make_plan(int M, int N, int K, LowlatPlan& p) {
-  const auto kern = w4a4_lowlat_kernel<FUSED, HB>;
+  const auto kern = w4a4_lowlat_kernel<FUSED, HB, CHAN>;
   const int nkb = K / 128;
   const int S = (nkb + kMaxKb - 1) / kMaxKb;
   if (S < 1 || S > kMaxCluster) return false;
@@ -615,16 +629,17 @@ bool make_plan(int M, int N, int K, LowlatPlan& p) {
   return true;
 }
 
-template <bool FUSED, int HB>
+template <bool FUSED, int HB, bool CHAN = false>
 vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const uint8_t* xq_in, const float* sx,
                            uint8_t* xq_ws, const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y,
-                           int M, int N, int K, int* status, cudaStream_t st, int sx_step = 1) {
+                           int M, int N, int K, int* status, cudaStream_t st, int sx_step = 1,
+                           const float* chan = nullptr) {
   cudaError_t ae = cudaSuccess;
-  set_attrs_once<FUSED, HB>(&ae);
+  set_attrs_once<FUSED, HB, CHAN>(&ae);
   if (ae != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a4 low-latency: cudaFuncSetAttribute: %s", cudaGetErrorString(ae));
   LowlatPlan p;
-  if (!make_plan<FUSED, HB>(M, N, K, p))
+  if (!make_plan<FUSED, HB, CHAN>(M, N, K, p))
     return vqlin::fail(VQLIN_ERR_UNSUPPORTED_SHAPE, "w4a4 low-latency: no plan for M=%d N=%d K=%d", M, N, K);
   const uint8_t* codes = FUSED ? xq_ws : xq_in;
   CUtensorMap tmW, tmXq;
@@ -637,7 +652,8 @@ vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const u
   if (!ok) return vqlin::fail(VQLIN_ERR_CUDA, "w4a4 low-latency: tensor map encoding failed (M=%d N=%d K=%d)", M, N, K);
 
   LowlatArgs a;
-  a.X = X; a.static_scale = static_scale; a.sx = sx; a.sx_step = sx_step; a.sw = sw; a.bias = bias; a.Y = Y;
+  a.X = X; a.chan = chan; a.static_scale = static_scale; a.sx = sx; a.sx_step = sx_step; a.sw = sw; a.bias = bias;
+  a.Y = Y;
   a.xq = xq_ws;
   a.status = status; a.M = M; a.N = N; a.K = K; a.bt = p.bt; a.nkb = K / 128; a.cn = p.cn;
   a.tmem_cols = p.cols; a.rows_per = p.rows_per; a.issuers = p.issuers; a.wait_limit_ns = kWaitLimitNs;
@@ -656,7 +672,7 @@ vqlin_status launch_lowlat(const uint16_t* X, const float* static_scale, const u
   attr[1].val.programmaticStreamSerializationAllowed = vqlin::pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = vqlin::launched(cudaLaunchKernelEx(&cfg, w4a4_lowlat_kernel<FUSED, HB>, tmW, tmXq, a));
+  const cudaError_t e = vqlin::launched(cudaLaunchKernelEx(&cfg, w4a4_lowlat_kernel<FUSED, HB, CHAN>, tmW, tmXq, a));
   if (e != cudaSuccess)
     return vqlin::fail(VQLIN_ERR_CUDA, "w4a4 low-latency launch (grid %d x %d x %d, cluster %d x %d, %zu B): %s",
                        p.tiles_n_pad, p.tiles_m, p.S, p.cn, p.S, p.dyn, cudaGetErrorString(e));
@@ -669,8 +685,15 @@ namespace vqlin {
 
 vqlin_status launch_w4a4_static_lowlat(const uint16_t* X, const float* static_scale, int hb, uint8_t* xq_ws,
                                        const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y, int M,
-                                       int N, int K, int* status, cudaStream_t st) {
+                                       int N, int K, int* status, cudaStream_t st, const float* chan) {
   if (M == 0 || N == 0) return VQLIN_OK;
+  if (chan != nullptr) {
+    if (hb == 64)
+      return launch_lowlat<true, 64, true>(X, static_scale, nullptr, nullptr, xq_ws, wq, sw, bias, Y, M, N, K, status,
+                                           st, 1, chan);
+    return launch_lowlat<true, 128, true>(X, static_scale, nullptr, nullptr, xq_ws, wq, sw, bias, Y, M, N, K, status,
+                                          st, 1, chan);
+  }
   if (hb == 64)
     return launch_lowlat<true, 64>(X, static_scale, nullptr, nullptr, xq_ws, wq, sw, bias, Y, M, N, K, status, st);
   return launch_lowlat<true, 128>(X, static_scale, nullptr, nullptr, xq_ws, wq, sw, bias, Y, M, N, K, status, st);

@@ -314,9 +314,10 @@ vqlin_status vqlin_debug_gemm_w4a8_s32(const uint16_t* xq, const uint8_t* wq, in
   return linear_int(8, xq, nullptr, wq, nullptr, nullptr, nullptr, acc, M, N, K, stream, true);
 }
 
-vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale, int hadamard_block,
-                                      const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y,
-                                      uint8_t* xq_out, int M, int N, int K, void* stream) {
+// The static-scale W4A4 projection, optionally with channel scaling (chan).
+static vqlin_status linear_w4a4_static_impl(const uint16_t* X, const float* static_scale, const float* chan,
+                                     int hadamard_block, const uint8_t* wq, const float* sw, const uint16_t* bias,
+                                     uint16_t* Y, uint8_t* xq_out, int M, int N, int K, void* stream) {
   REQUIRE(M >= 0 && N >= 0 && K > 0, VQLIN_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", M, N, K);
   REQUIRE(hadamard_block == 64 || hadamard_block == 128, VQLIN_ERR_INVALID_ARG,
           "hadamard_block must be 64 or 128 (got %d)", hadamard_block);
@@ -325,17 +326,19 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
   if (M == 0 || N == 0) return VQLIN_OK;
   REQUIRE_PTR(X); REQUIRE_PTR(static_scale); REQUIRE_PTR(wq); REQUIRE_PTR(sw); REQUIRE_PTR(Y); REQUIRE_PTR(xq_out);
   REQUIRE_ALIGNED(X); REQUIRE_ALIGNED(wq); REQUIRE_ALIGNED(Y); REQUIRE_ALIGNED(xq_out);
+  if (chan != nullptr) REQUIRE_ALIGNED(chan);
   int* status = vqlin::device_status_word();
   REQUIRE(status != nullptr, VQLIN_ERR_CUDA, "no device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K <= vqlin::kLowlatMaxK && M <= vqlin::kLowlatMaxM && vqlin::lowlat_one_wave(true, hadamard_block, M, N, K)) {
     if (!vqlin::static_two_launch(K))
       return vqlin::launch_w4a4_static_lowlat(X, static_scale, hadamard_block, xq_out, wq, sw, bias, Y, M, N, K,
-                                              status, st);
+                                              status, st, chan);
     if (vqlin::lowlat_one_wave(false, 128, M, N, K)) {
       // long K: the activation kernel, then the few-token GEMM on its codes
       vqlin_status r = vqlin::check_launch(
-          vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st), "act_hadamard_quant");
+          vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st, chan),
+          "act_hadamard_quant");
       if (r != VQLIN_OK) return r;
       return vqlin::launch_w4a4_codes_lowlat(xq_out, static_scale, wq, sw, bias, Y, M, N, K, status, st, 0);
     }
@@ -343,9 +346,25 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
   // longer K or more than one wave: the activation kernel writes the codes,
   // the throughput GEMM uses them
   vqlin_status r = vqlin::check_launch(
-      vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st), "act_hadamard_quant");
+      vqlin::launch_act_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, nullptr, st, chan),
+      "act_hadamard_quant");
   if (r != VQLIN_OK) return r;
   return vqlin::launch_int_gemm_static_scale(xq_out, static_scale, wq, sw, bias, Y, M, N, K, status, st);
+}
+
+vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_scale, int hadamard_block,
+                                      const uint8_t* wq, const float* sw, const uint16_t* bias, uint16_t* Y,
+                                      uint8_t* xq_out, int M, int N, int K, void* stream) {
+  return linear_w4a4_static_impl(X, static_scale, nullptr, hadamard_block, wq, sw, bias, Y, xq_out, M, N, K, stream);
+}
+
+vqlin_status vqlin_linear_w4a4_static_scaled(const uint16_t* X, const float* static_scale,
+                                             const float* channel_scale, int hadamard_block, const uint8_t* wq,
+                                             const float* sw, const uint16_t* bias, uint16_t* Y, uint8_t* xq_out,
+                                             int M, int N, int K, void* stream) {
+  if (M > 0 && N > 0) REQUIRE_PTR(channel_scale);
+  return linear_w4a4_static_impl(X, static_scale, channel_scale, hadamard_block, wq, sw, bias, Y, xq_out, M, N, K,
+                                 stream);
 }
 
 vqlin_status vqlin_debug_gemm_s32(int bits, const void* xq, const void* wq, int32_t* acc, int M, int N, int K,

@@ -204,8 +204,10 @@ vqlin_status vqlin_linear_w4a8(const uint16_t* xq, const float* sx, const uint8_
  * rotation and native integer execution).  Computes exactly what
  * vqlin_act_hadamard_quant(X, M, K, 4, hadamard_block, static_scale, xq_out, s)
  * followed by vqlin_linear_w4a4(xq_out, s, wq, sw, bias, Y, M, N, K) computes
- * (the same codes bit for bit, hence the same Y), in one kernel when
- * K <= 16384.  The kernel rotates and quantizes each activation tile once per
+ * (the same codes bit for bit, hence the same Y), in one kernel for up to 128
+ * tokens when K < 4096 and the plan's clusters fit in one wave, otherwise as
+ * the activation kernel followed by a GEMM on its codes (two launches).  The
+ * one-launch kernel rotates and quantizes each activation tile once per
  * thread-block cluster, not once per CTA: the cluster's CTAs write the codes to
  * xq_out, meet at a cluster barrier and read the codes of their K range back
  * from L2.  So xq_out is both the code output and the kernel's exchange buffer.
@@ -220,6 +222,25 @@ vqlin_status vqlin_linear_w4a4_static(const uint16_t* X, const float* static_sca
                                       int hadamard_block, const uint8_t* wq, const float* sw,
                                       const uint16_t* bias, uint16_t* Y, uint8_t* xq_out,
                                       int M, int N, int K, void* stream);
+
+/*
+ * vqlin_linear_w4a4_static with channel scaling (FoldQuantVLA abstract:
+ * channel scaling combined with the block Hadamard transform): the
+ * activations are divided by channel_scale[k] (IEEE float32 division of each
+ * loaded value) before the rotation and static-scale quantization, on chip in
+ * the one-launch kernel; wq must be quantized from W . diag(c) with the same c
+ * (vqlin_quantize_weights_rtn_scaled), so that the projection stays x . W^T.
+ * Computes exactly what vqlin_act_hadamard_quant_scaled(X, M, K, 4,
+ * hadamard_block, channel_scale, static_scale, xq_out, s) followed by
+ * vqlin_linear_w4a4 computes (same codes bit for bit, same Y).
+ * channel_scale: float [K] on the device, positive, finite, 16-byte aligned;
+ * VQLIN_ERR_INVALID_ARG if null.  Other arguments, layouts and errors as
+ * vqlin_linear_w4a4_static.
+ */
+vqlin_status vqlin_linear_w4a4_static_scaled(const uint16_t* X, const float* static_scale,
+                                             const float* channel_scale, int hadamard_block, const uint8_t* wq,
+                                             const float* sw, const uint16_t* bias, uint16_t* Y, uint8_t* xq_out,
+                                             int M, int N, int K, void* stream);
 
 /*
  * The same projection as vqlin_linear_w4a4_static, for callers that cannot

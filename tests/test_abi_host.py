@@ -86,6 +86,15 @@ def test_launch_count_is_host_side(lib):
     assert lib.vqlin_kernel_launch_count(None) == INVALID
 
 
+def test_static_scaled_rejects_bad_arguments(lib):
+    f = lib.vqlin_linear_w4a4_static_scaled
+    assert f(A, A, None, 128, A, A, None, A, A, 16, 256, 256, None) == INVALID      # null channel scale
+    assert f(A, A, A + 4, 128, A, A, None, A, A, 16, 256, 256, None) == MISALIGNED
+    assert f(A, A, A, 96, A, A, None, A, A, 16, 256, 256, None) == INVALID          # Hadamard block
+    assert f(A, A, A, 128, A, A, None, A, A, 16, 256, 192, None) == UNSUPPORTED     # K % 128
+    assert f(A, A, None, 128, A, A, None, A, A, 0, 256, 256, None) == OK            # empty: no-op
+
+
 def test_linear_rejects_bad_arguments(lib):
     assert lib.vqlin_linear_w4a4(A, A, A, A, None, A, 16, 16, 192, None) == UNSUPPORTED
     assert lib.vqlin_linear_w8a8(A, A, A, A, None, A, 16, 16, 96, None) == UNSUPPORTED

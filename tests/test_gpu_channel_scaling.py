@@ -105,3 +105,35 @@ def test_unit_channel_scale_is_the_plain_path():
         q1, s1 = vq.act_hadamard_quant(to_dev_bf16(Xb), bits, 128, channel_scale=one)
         q0, s0 = vq.act_hadamard_quant(to_dev_bf16(Xb), bits, 128)
         assert torch.equal(q1, q0) and torch.equal(s1, s0)
+
+
+# (M, N, K, hb): one launch (quantized on chip, clusters of 8 and 16), the
+# activation kernel + few-token GEMM at long K, and + throughput GEMM beyond
+# 128 tokens
+STATIC_SCALED = [(50, 1024, 1024, 128), (50, 3072, 1024, 64), (16, 256, 256, 64), (50, 1024, 4096, 128),
+                 (300, 512, 1024, 128)]
+
+
+@pytest.mark.parametrize("case", STATIC_SCALED, ids=lambda c: "%dx%dx%d-b%d" % c)
+def test_static_scale_with_channel_scaling(case):
+    # the static-scale projection with channel scaling: the same codes and Y as
+    # the activation kernel (static scale, channel factors) + the W4A4 GEMM,
+    # bit for bit, and within 1e-3 of the oracle
+    M, N, K, hb = case
+    Xb, Wb, c = _case(M, N, K, 231)
+    cd = torch.from_numpy(c).to(DEV)
+    c64 = c.astype(np.float64)
+    s = np.float32(o.calibrate_static_scale([activations(M, K, n_outliers=max(1, K // 100), outlier_scale=40,
+                                                         seed=234, tags=("cs", M, K))], 4, hb))
+    st = torch.tensor([s], dtype=torch.float32, device=DEV)
+    X = to_dev_bf16(Xb)
+    wq, sw = vq.quantize_weights_rtn(to_dev_bf16(Wb), 4, True, 0, hb, channel_scale=cd)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    y = vq.linear_w4a4_static(X, st, wq, sw, hb, xq_out=xq, channel_scale=cd)
+    vq.get_last_device_error()
+    xq2, sx2 = vq.act_hadamard_quant(X, 4, hb, static_scale=st, channel_scale=cd)
+    np.testing.assert_array_equal(xq.cpu().numpy(), xq2.cpu().numpy())
+    np.testing.assert_array_equal(bf16_bits(y), bf16_bits(vq.linear_w4a4(xq2, sx2, wq, sw)))
+    ref = sf.linear_quantized_scaled(Xb, Wb, 4, hb, c=c64, static_scale=s)
+    a, r = o.bf16_to_f64(bf16_bits(y)), o.bf16_to_f64(ref["y"])
+    assert np.linalg.norm(a - r) / np.linalg.norm(r) <= 1e-3
